@@ -1,0 +1,398 @@
+"""Benchmark of the fused linear + cross-entropy forward + backward on GB300.
+
+One step = one forward and one backward pass of the whole path (label scan and
+indexed dot, tensor-core linear-LSE, merge and reduction, dZ recompute, dW and dH)
+over one synthetic batch.  Default workload: the Llama-3-shaped head, N=8192 tokens,
+Hd=4096, V=128256, bf16, Zipf(1.1) labels with 5% ignored, mean reduction.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config llama3] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own batch (weak scaling, no collective in
+the data path); rank 0 prints one JSON line.  ``--impl reference`` times the fp64 CPU
+oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused linear-CE fwd+bwd tokens/s at 1 GB300; % of bf16 tensor peak; peak extra MB"
+L2_BYTES = 129 * 10**6
+
+# DRAM traffic per launch of the dominant kernel class from one ncu capture, keyed by
+# the hash of the kernel sources it was taken on (null once the sources change).
+MEASURED_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "linear_cross_entropy_indexed_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    sm_max=d.get("sm_max_mhz"), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, sm_max=2070.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "flce_clocks_%d_%d.csv" % (os.getpid(), device_index))
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+        return False
+
+    def summary(self, sm_max_default=None):
+        out = {"sm_mhz": None, "sm_max_mhz": sm_max_default, "reasons": [], "samples": 0}
+        if self.proc is None or not os.path.exists(self.path):
+            out["reasons"] = ["clock sampling unavailable"]
+            return out
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if sm:
+            out.update(sm_mhz=statistics.median(sm), sm_max_mhz=max(smax), samples=len(sm))
+        out["reasons"] = sorted(reasons)
+        return out
+
+
+# ---------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def workload_desc(w) -> str:
+    s = "%s: N=%d tokens, Hd=%d, V=%d, labels %s" % (w.name, w.N, w.Hd, w.V, w.labels)
+    if w.softcap > 0:
+        s += ", softcap %.1f" % w.softcap
+    return s
+
+
+def oracle_sample_step(Hf, Wf, y, w):
+    import oracle as O
+    ref = O.forward(Hf, Wf, y, w.ignore_index, w.softcap, w.reduction)
+    O.backward(Hf, Wf, y, ref.lse, w.ignore_index, w.softcap, w.reduction, 1.0)
+    return ref
+
+
+def blas_threads() -> int:
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(w, sample_tokens: int, repeats: int = 1):
+    """Time the fp64 oracle (as it stands) on the first `sample_tokens` rows of the
+    workload: a full forward + backward of that smaller batch with the whole W."""
+    import oracle as O
+    import synthetic as S
+    Hb = S.make_H(w, rows=slice(0, sample_tokens))
+    y = S.make_labels(w)[:sample_tokens]
+    Hf = O.widen_bf16(Hb)
+    Wf = O.widen_bf16(S.make_W(w))
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle_sample_step(Hf, Wf, y, w)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return dict(value=sample_tokens / t, unit="tokens/s", cores=blas_threads(), kind="oracle",
+                sample="first %d of %d tokens of %s, full W [%d x %d]; fp64 forward + backward, %d run(s), "
+                       "median %.2f s" % (sample_tokens, w.N, w.name, w.V, w.Hd, repeats, t),
+                seconds=t)
+
+
+# ---------------------------------------------------------------------------- reference arm
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle as O
+    import synthetic as S
+    n = args.ref_sample
+    Hf = O.widen_bf16(S.make_H(w, rows=slice(0, n)))
+    y = S.make_labels(w)[:n]
+    Wf = O.widen_bf16(S.make_W(w))
+    for _ in range(args.warmup):
+        oracle_sample_step(Hf, Wf, y, w)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_step(Hf, Wf, y, w)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "sample_tokens_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": "first %d tokens of %s per step, full W" % (n, w.name)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- our arm
+def run_ours(args, w):
+    import torch
+    import synthetic as S
+    import linear_cross_entropy_indexed_gb300 as F
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks = load_peaks()
+
+    # inputs: each rank its own batch (seed offset by rank), resident in HBM
+    wr = S.scaled(w.name, seed=w.seed + 1000 * rank) if rank else w
+    Hb, Wb, yb = S.make_H(wr), S.make_W(wr), S.make_labels(wr)
+    to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(dev)
+    H, W = to_dev(Hb), to_dev(Wb)
+    y = torch.from_numpy(yb).to(dev)
+    N, Hd, V = w.N, w.Hd, w.V
+    red = w.reduction
+    budget = args.chunk_budget
+    ws_bytes = max(F.forward_workspace_size(N, Hd, V), F.backward_workspace_size(N, Hd, V, budget))
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    dH = torch.empty_like(H)
+    dW = torch.empty_like(W)
+    g = torch.ones(1, dtype=torch.float32, device=dev)
+
+    def step():
+        loss, lse, counts, _ = F.flce_forward(H, W, y, w.ignore_index, w.softcap, red, workspace=workspace)
+        F.flce_backward(H, W, y, lse, counts, g, w.ignore_index, w.softcap, red, budget, workspace=workspace,
+                        dH=dH, dW=dW)
+        return loss, counts
+
+    for _ in range(args.warmup):
+        loss, counts = step()
+    torch.cuda.synchronize()
+    F.check_counts(counts)
+
+    # timed region: inputs (W 1 GB) larger than L2, so no flush is needed between steps
+    stream = torch.cuda.current_stream(dev)
+    n_launch0 = F.launch_count()
+    per_step = None
+    sink = F.EventSink(capacity=args.steps * 200)
+    with ClockSampler(dev.index) as clk:
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with sink:
+            e0.record(stream)
+            for _ in range(args.steps):
+                loss, counts = step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+    launches = F.launch_count() - n_launch0
+    ms = e0.elapsed_time(e1) / args.steps
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    F.check_counts(counts)
+    clocks = clk.summary(peaks["sm_max"])
+
+    # per kernel class time inside the timed region (events on the launch stream)
+    per_class = {}
+    for name, d in sink.durations_ms():
+        c = per_class.setdefault(name, [0, 0.0])
+        c[0] += 1
+        c[1] += d
+    flops_per_class = {"linear_lse": 2.0 * N * Hd * V, "dz": 2.0 * N * Hd * V, "dw": 2.0 * N * Hd * V,
+                       "dh": 2.0 * N * Hd * V}  # per step, summed over that class's launches
+    dom = max(per_class, key=lambda k: per_class[k][1])
+    roof = None
+    if dom in flops_per_class:
+        launches_dom, tot_ms = per_class[dom]
+        per_launch_ms = tot_ms / launches_dom
+        per_launch_flops = flops_per_class[dom] * args.steps / launches_dom
+        achieved = per_launch_flops / (per_launch_ms * 1e-3) / 1e12
+        h = kernel_source_hash()
+        traffic = MEASURED_TRAFFIC.get((dom, w.name, h))
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_sus"], "traffic": traffic,
+                "peak_kind": "bf16_tflops_sustained (%s)" % peaks["source"],
+                "frac_of_burst": achieved / peaks["bf16"], "launches": launches_dom,
+                "ms_per_launch": per_launch_ms}
+
+    # end to end through the public API with host buffers: pinned H/W/labels copied in,
+    # autograd forward + backward, loss read back every step
+    e2e = None
+    if not args.no_e2e:
+        Hh = torch.from_numpy(np.ascontiguousarray(Hb).view(np.int16)).view(torch.bfloat16).pin_memory()
+        Wh = torch.from_numpy(np.ascontiguousarray(Wb).view(np.int16)).view(torch.bfloat16).pin_memory()
+        yh = torch.from_numpy(yb).pin_memory()
+        Hd_ = torch.empty_like(H)
+        Wd_ = torch.empty_like(W)
+        yd_ = torch.empty_like(y)
+
+        def e2e_step():
+            Hd_.copy_(Hh, non_blocking=True)
+            Wd_.copy_(Wh, non_blocking=True)
+            yd_.copy_(yh, non_blocking=True)
+            Hx = Hd_.detach().requires_grad_(True)
+            Wx = Wd_.detach().requires_grad_(True)
+            loss = F.linear_cross_entropy(Hx, Wx, yd_, w.ignore_index, w.softcap, red, budget)
+            loss.backward()
+            return loss.item()
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        k2 = max(3, args.steps // 3)
+        t0 = time.perf_counter()
+        for _ in range(k2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_ms = 1e3 * (time.perf_counter() - t0) / k2
+        if ws > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        bi = Hh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 8
+        e2e = {"value": ws * N / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": 4, "ms_per_step": e2e_ms,
+               "path": "linear_cross_entropy() autograd, pinned host inputs copied every step, loss.item()"}
+
+    # peak extra device memory of one forward + backward through the public API
+    torch.cuda.synchronize()
+    Hx = H.detach().requires_grad_(True)
+    Wx = W.detach().requires_grad_(True)
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    loss = F.linear_cross_entropy(Hx, Wx, y, w.ignore_index, w.softcap, red, budget)
+    loss.backward()
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated(dev) - base
+    required = H.numel() * 2 + W.numel() * 2 + 4 * N + 4 + 24  # dH, dW, lse, loss, counts
+    peak_extra_mb = (peak - required) / 2**20
+    del Hx, Wx, loss
+
+    line = None
+    if rank == 0:
+        value = ws * N / (ms * 1e-3)
+        flops = 8.0 * N * Hd * V
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_desc(w), "global_batch": ws * N, "seq_len": 4096 if N >= 4096 else N,
+                       "parallelism": "dp%d" % ws if ws > 1 else "single",
+                       "l2": "inputs larger than L2 (W %.0f MiB > 129 MB); no flush" % (W.numel() * 2 / 2**20),
+                       "chunk_budget_bytes": budget or (1 << 30)},
+            "pct_bf16_peak": 100.0 * flops / (ms * 1e-3) / (peaks["bf16"] * 1e12),
+            "pct_bf16_peak_sustained": 100.0 * flops / (ms * 1e-3) / (peaks["bf16_sus"] * 1e12),
+            "peak_extra_mb": peak_extra_mb,
+            "workspace_mb": ws_bytes / 2**20,
+            "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roof,
+            "kernel_ms_per_step": {k: v[1] / args.steps for k, v in sorted(per_class.items())},
+        }
+    if ws > 1:
+        torch.distributed.barrier()
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = {k: v for k, v in cpu_baseline(w, args.cpu_sample).items() if k != "seconds"}
+    elif rank == 0:
+        line["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="llama3")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--chunk-budget", type=int, default=0)
+    ap.add_argument("--cpu-sample", type=int, default=256)
+    ap.add_argument("--ref-sample", type=int, default=64)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    import synthetic as S
+    w = S.WORKLOADS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,163 @@
+/*
+ * flce.h — C ABI of the fused LM-head linear + softmax cross-entropy for GB300 (sm_103a).
+ *
+ * The operation (per token row i, vocabulary entry v, hidden index k):
+ *   x_iv   = sum_k H[i,k] * W[v,k]                  logits Z = H W^T, never stored
+ *            (ai-infra-kb M011 "模型最后一层为什么也能占很多内存", §01: W is the [V, D]
+ *             output weight, Z = H W^T)
+ *   z_iv   = softcap > 0 ? softcap * tanh(x_iv / softcap) : x_iv
+ *            (Unsloth fused-CE notes, §4 forward: optional Gemma-2 softcap scaling)
+ *   lse_i  = log sum_v exp(z_iv), computed as max + log sum exp(z - max)
+ *            (ai-infra-kb M011, §03 stable per-row form; vocabulary tiles merged with
+ *             the running (max, sum) rule of §05)
+ *   loss_i = lse_i - z_{i,y_i} for valid rows, 0 for ignored rows
+ *            (Liger-CCE blog, §三 "CCE": LSE term plus the indexed-matmul target term)
+ *   mean   = sum_i loss_i / n_valid, divided once by the valid count
+ *            (ai-infra-kb M011, §04 and §07; Unsloth notes, §4 "n_items")
+ * Backward (ai-infra-kb M011, §06; Liger-CCE blog, §二 observation 1):
+ *   dZ_iv  = (exp(z_iv - lse_i) - [v == y_i]) * scale_i * (softcap > 0 ? 1 - tanh^2(x_iv/softcap) : 1)
+ *   dH     = dZ W   (summed over the vocabulary),   dW = dZ^T H   (summed over tokens)
+ *   scale_i = grad/n_valid (mean), grad (sum), grad_i (none); 0 for ignored rows.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked (device) are CUDA device pointers on the current device; the
+ *     library never allocates or frees memory.  The caller owns every buffer.
+ *   - H is [N, Hd] and W is [V, Hd], bf16, row-major and dense (row pitch = Hd
+ *     elements).  labels is [N] int64.  Base addresses must be 16-byte aligned and
+ *     Hd a multiple of 8 (TMA needs 16-byte row pitches).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
+ *     enqueued on it asynchronously; no call synchronises the host except on an
+ *     argument error, which is detected before anything is enqueued.
+ *   - A label equal to ignore_index is ignored.  A label outside [0, V) that is not
+ *     ignore_index is "bad": it is counted in counts[1] and the row is treated as
+ *     ignored (nothing traps on the device).
+ *   - Mean with n_valid == 0 gives loss 0 and zero gradients; counts[0] == 0 tells
+ *     the caller.  N == 0 is allowed (loss 0, counts 0, dW zeroed).
+ *   - Results are deterministic: every reduction runs in a fixed order, so two calls
+ *     on the same device with the same arguments give bitwise-identical outputs.
+ *   - Device-side bounded waits that expire set bits in counts[2]
+ *     (FLCE_DEVERR_*); the kernels then stop early instead of hanging.
+ *   - Kernels are built for sm_103a only; other devices get FLCE_ERR_UNSUPPORTED.
+ */
+#ifndef FLCE_H_
+#define FLCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FLCE_API __attribute__((visibility("default")))
+#else
+#define FLCE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum flce_status {
+  FLCE_OK = 0,
+  FLCE_ERR_ARG = 1,          /* null pointer, negative size, unknown reduction        */
+  FLCE_ERR_ALIGN = 2,        /* a base address is not 16-byte aligned, or Hd % 8 != 0 */
+  FLCE_ERR_WORKSPACE = 3,    /* workspace smaller than the size query, or not 256-B aligned */
+  FLCE_ERR_OVERFLOW = 4,     /* a size overflows 64-bit byte counts or the 2^31 TMA limits */
+  FLCE_ERR_CUDA = 5,         /* a CUDA runtime call failed; see flce_last_cuda_error() */
+  FLCE_ERR_UNSUPPORTED = 6   /* device is not sm_103, or a feature not built (filtering) */
+} flce_status;
+
+typedef enum flce_reduction {
+  FLCE_REDUCTION_MEAN = 0,   /* loss[0] = sum of valid losses / n_valid (0 if n_valid == 0) */
+  FLCE_REDUCTION_SUM = 1,    /* loss[0] = sum of valid losses                               */
+  FLCE_REDUCTION_NONE = 2    /* loss[i] = per-row loss, 0 for ignored rows                  */
+} flce_reduction;
+
+/* counts[2] bits */
+#define FLCE_DEVERR_WAIT_TIMEOUT 1u  /* an mbarrier wait exceeded its limit */
+
+/* Bytes of scratch that flce_forward needs for these sizes (0 when N == 0 is fine).
+   Returns 0 and sets no error for invalid sizes; flce_forward reports those. */
+FLCE_API size_t flce_forward_workspace_size(int64_t N, int64_t Hd, int64_t V);
+
+/* Bytes of scratch that flce_backward needs.  The backward walks the vocabulary in
+   chunks of Vc columns and keeps one bf16 [N, Vc] dZ chunk plus an fp32 [N, Hd] dH
+   accumulator (the latter only when there is more than one chunk).
+   chunk_budget_bytes bounds the dZ chunk (0 = default 1 GiB); the same value must be
+   passed to flce_backward. */
+FLCE_API size_t flce_backward_workspace_size(int64_t N, int64_t Hd, int64_t V, size_t chunk_budget_bytes);
+
+/* Forward: loss, per-row LSE (saved for the backward), target logits and counts.
+ *   H            (device) bf16 [N, Hd]
+ *   W            (device) bf16 [V, Hd]
+ *   labels       (device) int64 [N]
+ *   ignore_index label value that marks an ignored row (PyTorch default -100)
+ *   softcap      tanh logit softcap c; <= 0 turns it off
+ *   reduction    flce_reduction
+ *   loss         (device) fp32 [1] for MEAN/SUM, [N] for NONE
+ *   lse          (device) fp32 [N], LSE of every row (ignored rows included)
+ *   target_logit (device) fp32 [N] or NULL: z_{i,y_i} (capped), 0 for ignored rows
+ *   counts       (device) int64 [3]: n_valid, n_bad, device error bits (written)
+ *   workspace    (device) >= flce_forward_workspace_size() bytes, 256-byte aligned
+ *   stream       cudaStream_t
+ * Cites: Liger-CCE blog, §三 (indexed dot for the target, tiled linear-LSE for the
+ * denominator); ai-infra-kb M011, §05 (tile merge). */
+FLCE_API flce_status flce_forward(const void* H, const void* W, const int64_t* labels,
+                         int64_t N, int64_t Hd, int64_t V, int64_t ignore_index,
+                         float softcap, int reduction,
+                         float* loss, float* lse, float* target_logit, int64_t* counts,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward: dH and dW from the saved LSE, recomputing the logits tile by tile.
+ *   H, W, labels, N, Hd, V, ignore_index, softcap, reduction: as in the forward call
+ *   lse          (device) fp32 [N] from flce_forward
+ *   counts       (device) int64 [3] from flce_forward; counts[0] (n_valid) scales the
+ *                mean; error bits are OR-ed into counts[2]
+ *   grad_out     (device) fp32 [1] (MEAN/SUM) or [N] (NONE): upstream gradient
+ *   filter_threshold  must be 0 (exact backward); tile skipping is not built
+ *   dH           (device) bf16 [N, Hd] (written)
+ *   dW           (device) bf16 [V, Hd] (written, every row)
+ *   workspace    (device) >= flce_backward_workspace_size(N, Hd, V, chunk_budget_bytes)
+ *   chunk_budget_bytes  as passed to the size query (0 = default)
+ * Cites: ai-infra-kb M011, §06 (recompute the logit tile, p = exp(z - lse),
+ * dH summed over vocabulary tiles, dW over all valid tokens); Unsloth notes, §4
+ * backward (softcap derivative 1 - tanh^2). */
+FLCE_API flce_status flce_backward(const void* H, const void* W, const int64_t* labels,
+                          const float* lse, int64_t* counts,
+                          int64_t N, int64_t Hd, int64_t V, int64_t ignore_index,
+                          float softcap, int reduction, const float* grad_out,
+                          float filter_threshold, void* dH, void* dW,
+                          void* workspace, size_t workspace_bytes, size_t chunk_budget_bytes,
+                          void* stream);
+
+/* Human-readable text for a flce_status value. */
+FLCE_API const char* flce_strerror(int status);
+
+/* The cudaError_t value behind the last FLCE_ERR_CUDA returned on this thread. */
+FLCE_API int flce_last_cuda_error(void);
+
+/* Instrumentation (host side, per calling thread).
+ * flce_launch_count: number of kernels this thread has launched through the library.
+ * flce_set_event_sink: while capacity > 0, every kernel launch k (in launch order) is
+ *   bracketed by cudaEventRecord(start_events[k]) / cudaEventRecord(end_events[k]) on
+ *   the launch stream and kernel_ids[k] receives its FLCE_KERNEL_* id; launches past
+ *   capacity are not recorded.  Events are cudaEvent_t created by the caller.
+ *   capacity 0 turns the sink off.  Returns 0.
+ * flce_event_sink_used: number of launches recorded since the last flce_set_event_sink. */
+#define FLCE_KERNEL_LABEL_DOT 0   /* label scan + indexed dot (target logits)          */
+#define FLCE_KERNEL_LINEAR_LSE 1  /* tensor-core H W^T tiles -> per-group (max, sum)   */
+#define FLCE_KERNEL_LSE_MERGE 2   /* fixed-order merge -> lse, per-row loss, row sums  */
+#define FLCE_KERNEL_REDUCE 3      /* fixed-order total, counts, mean                   */
+#define FLCE_KERNEL_BWD_PREP 4    /* per-row scale / label / lse for the backward      */
+#define FLCE_KERNEL_DZ 5          /* tensor-core recompute of Z -> bf16 dZ chunk       */
+#define FLCE_KERNEL_DW 6          /* tensor-core dW chunk = dZ^T H                     */
+#define FLCE_KERNEL_DH 7          /* tensor-core dH += dZ W_chunk                      */
+#define FLCE_KERNEL_ZERO 8        /* zero fill (dW when N == 0)                        */
+FLCE_API uint64_t flce_launch_count(void);
+FLCE_API int flce_set_event_sink(void* const* start_events, void* const* end_events, int* kernel_ids,
+                        int capacity);
+FLCE_API int flce_event_sink_used(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H_ */

@@ -1,0 +1,247 @@
+"""Fused LM-head linear + softmax cross-entropy for GB300 (sm_103a).
+
+A thin Python binding over the C ABI in ``include/flce.h`` (``libflce.so`` built in
+tree by ``_build.py``).  This file only marshals arguments: PyTorch provides device
+memory and the current stream; every step of the computation runs in the library's
+CUDA kernels.  There is no CPU fallback: if the library is missing or the device is
+not an sm_103 GPU, the calls raise.
+
+User entry point::
+
+    loss = linear_cross_entropy(hidden, lm_head_weight, labels,
+                                ignore_index=-100, softcap=0.0, reduction="mean")
+    loss.backward()        # dH and dW through the fused backward
+
+``hidden`` is [..., Hd] bf16, ``lm_head_weight`` is [V, Hd] bf16 (the layout of a
+PyTorch ``nn.Linear(Hd, V).weight``), ``labels`` is [...] int64 and already shifted
+for next-token prediction.  The N x V logits are never materialised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "linear_cross_entropy", "flce_forward", "flce_backward", "forward_workspace_size",
+    "backward_workspace_size", "FlceError", "check_counts", "library", "launch_count",
+    "EventSink", "KERNEL_NAMES",
+]
+
+REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
+KERNEL_NAMES = {0: "label_dot", 1: "linear_lse", 2: "lse_merge", 3: "reduce", 4: "bwd_prep",
+                5: "dz", 6: "dw", 7: "dh", 8: "zero"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FlceError(RuntimeError):
+    pass
+
+
+def library() -> ctypes.CDLL:
+    """The loaded ``libflce.so``; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                raise FlceError("libflce.so is not built (run __graft_entry__.build() or "
+                                "python -m linear_cross_entropy_indexed_gb300._build)")
+            lib = ctypes.CDLL(_build.LIB)
+            i64, sz, vp, f32, i32 = (ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p,
+                                     ctypes.c_float, ctypes.c_int)
+            lib.flce_forward_workspace_size.argtypes = [i64, i64, i64]
+            lib.flce_forward_workspace_size.restype = sz
+            lib.flce_backward_workspace_size.argtypes = [i64, i64, i64, sz]
+            lib.flce_backward_workspace_size.restype = sz
+            lib.flce_forward.argtypes = [vp, vp, vp, i64, i64, i64, i64, f32, i32, vp, vp, vp, vp, vp, sz, vp]
+            lib.flce_forward.restype = i32
+            lib.flce_backward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, i32, vp, f32, vp, vp,
+                                          vp, sz, sz, vp]
+            lib.flce_backward.restype = i32
+            lib.flce_strerror.argtypes = [i32]
+            lib.flce_strerror.restype = ctypes.c_char_p
+            lib.flce_last_cuda_error.restype = i32
+            lib.flce_launch_count.restype = ctypes.c_uint64
+            lib.flce_set_event_sink.argtypes = [vp, vp, vp, i32]
+            lib.flce_set_event_sink.restype = i32
+            lib.flce_event_sink_used.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        lib = library()
+        raise FlceError("flce: %s (status %d, cuda error %d)" % (
+            lib.flce_strerror(status).decode(), status, lib.flce_last_cuda_error()))
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _reduction(r) -> int:
+    if isinstance(r, int):
+        return r
+    try:
+        return REDUCTIONS[r]
+    except KeyError:
+        raise ValueError("reduction must be one of %s" % list(REDUCTIONS)) from None
+
+
+def forward_workspace_size(N: int, Hd: int, V: int) -> int:
+    return int(library().flce_forward_workspace_size(N, Hd, V))
+
+
+def backward_workspace_size(N: int, Hd: int, V: int, chunk_budget: int = 0) -> int:
+    return int(library().flce_backward_workspace_size(N, Hd, V, chunk_budget))
+
+
+def _check_inputs(H, W, labels):
+    for name, t in (("H", H), ("W", W), ("labels", labels)):
+        if not t.is_cuda:
+            raise FlceError("%s must be a CUDA tensor" % name)
+        if not t.is_contiguous():
+            raise FlceError("%s must be contiguous" % name)
+    if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise FlceError("H and W must be bfloat16")
+    if labels.dtype != torch.int64:
+        raise FlceError("labels must be int64")
+    if H.dim() != 2 or W.dim() != 2 or labels.dim() != 1:
+        raise FlceError("expected H [N, Hd], W [V, Hd], labels [N]")
+    if H.shape[1] != W.shape[1] or labels.shape[0] != H.shape[0]:
+        raise FlceError("shape mismatch: H %s, W %s, labels %s" % (tuple(H.shape), tuple(W.shape),
+                                                                     tuple(labels.shape)))
+    if not (H.device == W.device == labels.device):
+        raise FlceError("H, W and labels must be on one device")
+
+
+def flce_forward(H, W, labels, ignore_index: int = -100, softcap: float = 0.0, reduction="mean",
+                 want_target: bool = False, workspace=None):
+    """One forward call.  Returns (loss, lse, counts, target_or_None); loss is a
+    0-d tensor for mean/sum and [N] for none; counts = [n_valid, n_bad, error_bits]."""
+    _check_inputs(H, W, labels)
+    red = _reduction(reduction)
+    N, Hd = H.shape
+    V = W.shape[0]
+    dev = H.device
+    with torch.cuda.device(dev):
+        loss = torch.empty(N if red == 2 else 1, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+        counts = torch.empty(3, dtype=torch.int64, device=dev)
+        tgt = torch.empty(N, dtype=torch.float32, device=dev) if want_target else None
+        need = forward_workspace_size(N, Hd, V)
+        ws = workspace if workspace is not None else torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        _check(library().flce_forward(_p(H), _p(W), _p(labels), N, Hd, V, int(ignore_index), float(softcap), red,
+                                      _p(loss), _p(lse), _p(tgt), _p(counts), _p(ws), ws.numel(), _stream(dev)))
+    return (loss if red == 2 else loss[0]), lse, counts, tgt
+
+
+def flce_backward(H, W, labels, lse, counts, grad_out, ignore_index: int = -100, softcap: float = 0.0,
+                  reduction="mean", chunk_budget: int = 0, workspace=None, dH=None, dW=None):
+    """One backward call from the saved LSE and counts.  Returns (dH, dW) in bf16."""
+    _check_inputs(H, W, labels)
+    red = _reduction(reduction)
+    N, Hd = H.shape
+    V = W.shape[0]
+    dev = H.device
+    g = grad_out.to(device=dev, dtype=torch.float32).reshape(-1).contiguous()
+    if g.numel() != (N if red == 2 else 1):
+        raise FlceError("grad_out has %d elements" % g.numel())
+    with torch.cuda.device(dev):
+        dH = dH if dH is not None else torch.empty_like(H)
+        dW = dW if dW is not None else torch.empty_like(W)
+        need = backward_workspace_size(N, Hd, V, chunk_budget)
+        ws = workspace if workspace is not None else torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        _check(library().flce_backward(_p(H), _p(W), _p(labels), _p(lse), _p(counts), N, Hd, V, int(ignore_index),
+                                       float(softcap), red, _p(g), 0.0, _p(dH), _p(dW), _p(ws), ws.numel(),
+                                       int(chunk_budget), _stream(dev)))
+    return dH, dW
+
+
+def check_counts(counts) -> tuple[int, int]:
+    """Host check of a counts tensor (synchronises): raises on bad labels or on a
+    device-side wait timeout; returns (n_valid, n_bad)."""
+    c = counts.tolist()
+    if c[2] != 0:
+        raise FlceError("device error bits %#x (a bounded wait expired)" % c[2])
+    if c[1] != 0:
+        raise FlceError("%d labels outside [0, V) that are not ignore_index" % c[1])
+    return c[0], c[1]
+
+
+class _FusedLinearCrossEntropy(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, H, W, labels, ignore_index, softcap, reduction, chunk_budget):
+        loss, lse, counts, _ = flce_forward(H, W, labels, ignore_index, softcap, reduction)
+        ctx.save_for_backward(H, W, labels, lse, counts)
+        ctx.cfg = (ignore_index, softcap, reduction, chunk_budget)
+        return loss
+
+    @staticmethod
+    def backward(ctx, grad):
+        H, W, labels, lse, counts = ctx.saved_tensors
+        ignore_index, softcap, reduction, chunk_budget = ctx.cfg
+        dH, dW = flce_backward(H, W, labels, lse, counts, grad, ignore_index, softcap, reduction, chunk_budget)
+        return (dH if ctx.needs_input_grad[0] else None, dW if ctx.needs_input_grad[1] else None,
+                None, None, None, None, None)
+
+
+def linear_cross_entropy(hidden, weight, labels, ignore_index: int = -100, softcap: float = 0.0,
+                         reduction: str = "mean", chunk_budget: int = 0):
+    """Cross-entropy of ``hidden @ weight.T`` against ``labels`` without materialising
+    the logits.  ``hidden`` [..., Hd] bf16, ``weight`` [V, Hd] bf16, ``labels`` [...]
+    int64.  reduction: "mean" (over rows whose label is valid), "sum" or "none"."""
+    Hd = hidden.shape[-1]
+    H2 = hidden.reshape(-1, Hd)
+    y = labels.reshape(-1)
+    out = _FusedLinearCrossEntropy.apply(H2.contiguous(), weight.contiguous(), y.contiguous(), int(ignore_index),
+                                         float(softcap), reduction, int(chunk_budget))
+    if reduction == "none":
+        out = out.reshape(labels.shape)
+    return out
+
+
+def launch_count() -> int:
+    """Kernels launched through the library by this thread so far."""
+    return int(library().flce_launch_count())
+
+
+class EventSink:
+    """Bracket every library kernel launch with a pair of CUDA events (for timing
+    per kernel class on the launch stream).  Use as a context manager."""
+
+    def __init__(self, capacity: int):
+        self.capacity = capacity
+        self.start = [torch.cuda.Event(enable_timing=True) for _ in range(capacity)]
+        self.end = [torch.cuda.Event(enable_timing=True) for _ in range(capacity)]
+        for e in self.start + self.end:
+            e.record()  # materialise the underlying cudaEvent_t
+        self._s = (ctypes.c_void_p * capacity)(*[e.cuda_event for e in self.start])
+        self._e = (ctypes.c_void_p * capacity)(*[e.cuda_event for e in self.end])
+        self._ids = (ctypes.c_int * capacity)()
+        self.used = 0
+
+    def __enter__(self):
+        library().flce_set_event_sink(self._s, self._e, self._ids, self.capacity)
+        return self
+
+    def __exit__(self, *exc):
+        self.used = int(library().flce_event_sink_used())
+        library().flce_set_event_sink(None, None, None, 0)
+        return False
+
+    def durations_ms(self):
+        """[(kernel_name, ms)] for every recorded launch (call after a synchronize)."""
+        return [(KERNEL_NAMES.get(self._ids[k], str(self._ids[k])), self.start[k].elapsed_time(self.end[k]))
+                for k in range(self.used)]

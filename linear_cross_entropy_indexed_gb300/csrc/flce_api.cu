@@ -1,0 +1,419 @@
+// C-ABI entry points: argument checks, workspace planning, tensor-map encoding and
+// the launch sequence of the forward and backward passes.  All device work is
+// enqueued on the caller's stream; nothing here synchronises the host.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "flce.h"
+#include "internal.cuh"
+#include "small_kernels.cuh"
+
+namespace flce {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kLseGroup = 4;                         // vocabulary tiles per forward unit
+constexpr size_t kDefaultChunkBudget = size_t(1) << 30;  // bf16 dZ chunk bytes
+constexpr int kMaxDevices = 64;
+
+thread_local int t_last_cuda = 0;
+thread_local uint64_t t_launches = 0;
+struct EventSink {
+  void* const* start = nullptr;
+  void* const* end = nullptr;
+  int* ids = nullptr;
+  int cap = 0;
+  int used = 0;
+};
+thread_local EventSink t_sink;
+
+struct DeviceState {
+  bool initialized = false;
+  flce_status status = FLCE_OK;
+  int sms = 0;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool mul_ok(size_t a, size_t b, size_t* out) { return !__builtin_mul_overflow(a, b, out); }
+bool add_ok(size_t a, size_t b, size_t* out) { return !__builtin_add_overflow(a, b, out); }
+
+// Reserve `bytes` at 256-byte alignment; false on overflow.
+bool reserve(size_t* cursor, size_t bytes, size_t* offset) {
+  *offset = align_up(*cursor);
+  return add_ok(*offset, bytes, cursor);
+}
+
+flce_status cuda_fail(cudaError_t e) {
+  t_last_cuda = static_cast<int>(e);
+  return FLCE_ERR_CUDA;
+}
+
+// Launch bookkeeping: optional event pair around the launch, launch counter.
+template <class F>
+cudaError_t launch(int kernel_id, cudaStream_t st, F&& f) {
+  const bool rec = t_sink.cap > 0 && t_sink.used < t_sink.cap;
+  if (rec) cudaEventRecord(static_cast<cudaEvent_t>(t_sink.start[t_sink.used]), st);
+  cudaError_t e = f();
+  if (rec) {
+    cudaEventRecord(static_cast<cudaEvent_t>(t_sink.end[t_sink.used]), st);
+    t_sink.ids[t_sink.used] = kernel_id;
+    ++t_sink.used;
+  }
+  ++t_launches;
+  return e;
+}
+
+flce_status device_setup(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return FLCE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.initialized) {
+    int major = 0, minor = 0, count = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if (major != 10 || minor != 3) {
+      d.status = FLCE_ERR_UNSUPPORTED;
+    } else {
+      if ((e = set_gemm_smem_attributes_fwd()) != cudaSuccess) return cuda_fail(e);
+      if ((e = set_gemm_smem_attributes_bwd()) != cudaSuccess) return cuda_fail(e);
+      std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+          g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      });
+      d.status = g_encode ? FLCE_OK : FLCE_ERR_CUDA;
+    }
+    d.sms = count;
+    d.initialized = true;
+  }
+  *sms = d.sms;
+  return d.status;
+}
+
+// 2-D bf16 tensor map with 128-byte swizzle: dims {inner, outer}, row pitch in bytes.
+bool tmap_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
+             uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  std::memset(tm, 0, sizeof(*tm));
+  const CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int cdiv(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+// ------------------------------------------------------------------ planning
+struct FwdPlan {
+  int m_tiles = 0, v_tiles = 0, n_groups = 0, k_blocks = 0;
+  int dot_blocks = 0, merge_blocks = 0;
+  size_t off_pm = 0, off_ps = 0, off_t = 0, off_sums = 0, off_counts = 0, total = 0;
+};
+
+flce_status check_sizes(int64_t N, int64_t Hd, int64_t V) {
+  if (N < 0 || Hd <= 0 || V <= 0) return FLCE_ERR_ARG;
+  if (Hd % 8 != 0) return FLCE_ERR_ALIGN;
+  // TMA coordinates are int32 and the label is kept as int32 on the device.
+  const int64_t lim = (int64_t(1) << 31) - 512;
+  if (N > lim || Hd > lim || V > lim) return FLCE_ERR_OVERFLOW;
+  size_t b;
+  if (!mul_ok(size_t(N), size_t(Hd), &b) || !mul_ok(b, 4, &b)) return FLCE_ERR_OVERFLOW;
+  if (!mul_ok(size_t(V), size_t(Hd), &b) || !mul_ok(b, 4, &b)) return FLCE_ERR_OVERFLOW;
+  return FLCE_OK;
+}
+
+flce_status plan_forward(int64_t N, int64_t Hd, int64_t V, FwdPlan* p) {
+  flce_status s = check_sizes(N, Hd, V);
+  if (s != FLCE_OK) return s;
+  p->m_tiles = cdiv(N, kBM);
+  p->v_tiles = cdiv(V, kBN);
+  p->n_groups = cdiv(p->v_tiles, kLseGroup);
+  p->k_blocks = cdiv(Hd, kBK);
+  p->dot_blocks = static_cast<int>(std::min<int64_t>(std::max<int64_t>(cdiv(N, kDotWarps), 1), kDotMaxBlocks));
+  p->merge_blocks = std::max(cdiv(N, kMergeThreads), 1);
+  size_t cur = 0, part;
+  if (!mul_ok(size_t(p->n_groups), size_t(N), &part) || !mul_ok(part, 4, &part)) return FLCE_ERR_OVERFLOW;
+  if (!reserve(&cur, part, &p->off_pm) || !reserve(&cur, part, &p->off_ps) ||
+      !reserve(&cur, size_t(N) * 4, &p->off_t) || !reserve(&cur, size_t(p->merge_blocks) * 8, &p->off_sums) ||
+      !reserve(&cur, size_t(p->dot_blocks) * 8, &p->off_counts))
+    return FLCE_ERR_OVERFLOW;
+  p->total = align_up(cur);
+  return FLCE_OK;
+}
+
+struct BwdPlan {
+  int64_t Vc = 0;
+  int n_chunks = 0;
+  size_t off_rows = 0, off_dz = 0, off_dh = 0, total = 0;
+};
+
+flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, BwdPlan* p) {
+  flce_status s = check_sizes(N, Hd, V);
+  if (s != FLCE_OK) return s;
+  if (budget == 0) budget = kDefaultChunkBudget;
+  const int64_t v_round = int64_t(cdiv(V, kBN)) * kBN;
+  int64_t vc = N > 0 ? static_cast<int64_t>(budget / (size_t(N) * 2)) : v_round;
+  vc = vc / kBN * kBN;
+  if (vc < kBN) vc = kBN;
+  if (vc > v_round) vc = v_round;
+  p->Vc = vc;
+  p->n_chunks = cdiv(V, vc);
+  size_t cur = 0, dz, dh = 0;
+  if (!mul_ok(size_t(N), size_t(vc), &dz) || !mul_ok(dz, 2, &dz)) return FLCE_ERR_OVERFLOW;
+  if (p->n_chunks > 1 && (!mul_ok(size_t(N), size_t(Hd), &dh) || !mul_ok(dh, 4, &dh))) return FLCE_ERR_OVERFLOW;
+  if (!reserve(&cur, size_t(N) * sizeof(RowInfo), &p->off_rows) || !reserve(&cur, dz, &p->off_dz) ||
+      !reserve(&cur, dh, &p->off_dh))
+    return FLCE_ERR_OVERFLOW;
+  p->total = align_up(cur);
+  return FLCE_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace flce
+
+using namespace flce;
+
+extern "C" {
+
+size_t flce_forward_workspace_size(int64_t N, int64_t Hd, int64_t V) {
+  FwdPlan p;
+  return plan_forward(N, Hd, V, &p) == FLCE_OK ? p.total : 0;
+}
+
+size_t flce_backward_workspace_size(int64_t N, int64_t Hd, int64_t V, size_t chunk_budget_bytes) {
+  BwdPlan p;
+  return plan_backward(N, Hd, V, chunk_budget_bytes, &p) == FLCE_OK ? p.total : 0;
+}
+
+flce_status flce_forward(const void* H, const void* W, const int64_t* labels, int64_t N, int64_t Hd, int64_t V,
+                         int64_t ignore_index, float softcap, int reduction, float* loss, float* lse,
+                         float* target_logit, int64_t* counts, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  if (reduction < 0 || reduction > 2 || softcap != softcap) return FLCE_ERR_ARG;
+  FwdPlan pl;
+  flce_status s = plan_forward(N, Hd, V, &pl);
+  if (s != FLCE_OK) return s;
+  if (!W || !loss || !counts) return FLCE_ERR_ARG;
+  if (N > 0 && (!H || !labels || !lse || !workspace)) return FLCE_ERR_ARG;
+  if (!aligned(W, 16) || (H && !aligned(H, 16)) || !aligned(counts, 8) || (labels && !aligned(labels, 8)) ||
+      !aligned(loss, 4) || (lse && !aligned(lse, 4)) || (target_logit && !aligned(target_logit, 4)))
+    return FLCE_ERR_ALIGN;
+  if (N > 0 && (workspace_bytes < pl.total || !aligned(workspace, kAlign))) return FLCE_ERR_WORKSPACE;
+  int sms = 0;
+  if ((s = device_setup(&sms)) != FLCE_OK) return s;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(counts, 0, 3 * sizeof(int64_t), st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (N == 0) {
+    if (reduction != FLCE_REDUCTION_NONE && (e = cudaMemsetAsync(loss, 0, sizeof(float), st)) != cudaSuccess)
+      return cuda_fail(e);
+    return FLCE_OK;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* part_m = reinterpret_cast<float*>(ws + pl.off_pm);
+  float* part_s = reinterpret_cast<float*>(ws + pl.off_ps);
+  float* t_ws = reinterpret_cast<float*>(ws + pl.off_t);
+  double* sums = reinterpret_cast<double*>(ws + pl.off_sums);
+  int2* blk_counts = reinterpret_cast<int2*>(ws + pl.off_counts);
+  unsigned long long* err = reinterpret_cast<unsigned long long*>(counts + 2);
+  const auto* Hb = static_cast<const __nv_bfloat16*>(H);
+  const auto* Wb = static_cast<const __nv_bfloat16*>(W);
+
+  // (1) label scan + indexed dot
+  e = launch(FLCE_KERNEL_LABEL_DOT, st, [&] {
+    k_label_dot<<<pl.dot_blocks, 32 * kDotWarps, 0, st>>>(Hb, Wb, labels, N, Hd, V, ignore_index, softcap, t_ws,
+                                                          target_logit, blk_counts);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  // (2) tensor-core linear-LSE
+  CUtensorMap tmH, tmW;
+  if (!tmap_2d(&tmH, H, Hd, N, Hd * 2, kBK, kBM) || !tmap_2d(&tmW, W, Hd, V, Hd * 2, kBK, kBN))
+    return FLCE_ERR_CUDA;
+  Sched sc{};
+  sc.m_tiles = pl.m_tiles;
+  sc.n_tiles = pl.v_tiles;
+  sc.k_blocks = pl.k_blocks;
+  sc.group = kLseGroup;
+  sc.n_groups = pl.n_groups;
+  sc.units = pl.m_tiles * pl.n_groups;
+  sc.order = 0;
+  EpiLseParams lp{N, V, softcap, part_m, part_s};
+  const int grid = std::min(sc.units, sms);
+  e = launch(FLCE_KERNEL_LINEAR_LSE, st, [&] { return launch_linear_lse(tmH, tmW, sc, lp, err, grid, st); });
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  // (3) fixed-order merge, per-row loss, block sums
+  float* loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : nullptr;
+  e = launch(FLCE_KERNEL_LSE_MERGE, st, [&] {
+    k_lse_merge<<<pl.merge_blocks, kMergeThreads, 0, st>>>(part_m, part_s, pl.n_groups, N, t_ws, labels,
+                                                           ignore_index, V, lse, loss_rows, sums);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  // (4) totals, counts, mean
+  e = launch(FLCE_KERNEL_REDUCE, st, [&] {
+    k_reduce<<<1, 256, 0, st>>>(sums, pl.merge_blocks, blk_counts, pl.dot_blocks, reduction, loss, counts);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FLCE_OK;
+}
+
+flce_status flce_backward(const void* H, const void* W, const int64_t* labels, const float* lse, int64_t* counts,
+                          int64_t N, int64_t Hd, int64_t V, int64_t ignore_index, float softcap, int reduction,
+                          const float* grad_out, float filter_threshold, void* dH, void* dW, void* workspace,
+                          size_t workspace_bytes, size_t chunk_budget_bytes, void* stream) {
+  if (reduction < 0 || reduction > 2 || softcap != softcap || filter_threshold != filter_threshold)
+    return FLCE_ERR_ARG;
+  if (filter_threshold != 0.0f) return FLCE_ERR_UNSUPPORTED;
+  BwdPlan pl;
+  flce_status s = plan_backward(N, Hd, V, chunk_budget_bytes, &pl);
+  if (s != FLCE_OK) return s;
+  if (!W || !dW || !counts) return FLCE_ERR_ARG;
+  if (N > 0 && (!H || !labels || !lse || !grad_out || !dH || !workspace)) return FLCE_ERR_ARG;
+  if (!aligned(W, 16) || !aligned(dW, 16) || (H && !aligned(H, 16)) || (dH && !aligned(dH, 16)) ||
+      !aligned(counts, 8) || (labels && !aligned(labels, 8)) || (lse && !aligned(lse, 4)) ||
+      (grad_out && !aligned(grad_out, 4)))
+    return FLCE_ERR_ALIGN;
+  if (N > 0 && (workspace_bytes < pl.total || !aligned(workspace, kAlign))) return FLCE_ERR_WORKSPACE;
+  int sms = 0;
+  if ((s = device_setup(&sms)) != FLCE_OK) return s;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (N == 0) {  // no tokens: the weight gradient is an empty sum
+    e = cudaMemsetAsync(dW, 0, size_t(V) * size_t(Hd) * 2, st);
+    return e == cudaSuccess ? FLCE_OK : cuda_fail(e);
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  RowInfo* rows = reinterpret_cast<RowInfo*>(ws + pl.off_rows);
+  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_dz);
+  float* dh32 = pl.n_chunks > 1 ? reinterpret_cast<float*>(ws + pl.off_dh) : nullptr;
+  unsigned long long* err = reinterpret_cast<unsigned long long*>(counts + 2);
+
+  e = launch(FLCE_KERNEL_BWD_PREP, st, [&] {
+    k_bwd_prep<<<cdiv(N, 256), 256, 0, st>>>(labels, lse, counts, grad_out, reduction, N, V, ignore_index, rows);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  CUtensorMap tmH_k, tmW_k, tmH_mn, tmW_mn;
+  if (!tmap_2d(&tmH_k, H, Hd, N, Hd * 2, kBK, kBM) || !tmap_2d(&tmW_k, W, Hd, V, Hd * 2, kBK, kBN) ||
+      !tmap_2d(&tmH_mn, H, Hd, N, Hd * 2, 64, kBK) || !tmap_2d(&tmW_mn, W, Hd, V, Hd * 2, 64, kBK))
+    return FLCE_ERR_CUDA;
+
+  const int m_tiles_tok = cdiv(N, kBM);
+  const int d_tiles = cdiv(Hd, kBN);
+  for (int c = 0; c < pl.n_chunks; ++c) {
+    const int64_t v0 = int64_t(c) * pl.Vc;
+    const int64_t wc = std::min<int64_t>(pl.Vc, V - v0);
+    CUtensorMap tmDz_k, tmDz_mn;
+    if (!tmap_2d(&tmDz_k, dz, wc, N, pl.Vc * 2, kBK, kBM) || !tmap_2d(&tmDz_mn, dz, wc, N, pl.Vc * 2, 64, kBK))
+      return FLCE_ERR_CUDA;
+
+    // dZ chunk = f(H W_chunk^T)
+    Sched s4{};
+    s4.m_tiles = m_tiles_tok;
+    s4.n_tiles = cdiv(wc, kBN);
+    s4.k_blocks = cdiv(Hd, kBK);
+    s4.group = 1;
+    s4.n_groups = s4.n_tiles;
+    s4.units = s4.m_tiles * s4.n_groups;
+    s4.order = 0;
+    s4.b_n_off = static_cast<int>(v0);
+    EpiDzParams p4{N, V, v0, wc, pl.Vc, softcap, rows, dz};
+    e = launch(FLCE_KERNEL_DZ, st,
+               [&] { return launch_dz(tmH_k, tmW_k, s4, p4, err, std::min(s4.units, sms), st); });
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    // dW rows [v0, v0 + wc) = dZ_chunk^T H
+    Sched s5{};
+    s5.m_tiles = cdiv(wc, kBM);
+    s5.n_tiles = d_tiles;
+    s5.k_blocks = cdiv(N, kBK);
+    s5.group = 1;
+    s5.n_groups = d_tiles;
+    s5.units = s5.m_tiles * s5.n_groups;
+    s5.order = 1;
+    EpiDwParams p5{wc, v0, Hd, static_cast<__nv_bfloat16*>(dW)};
+    e = launch(FLCE_KERNEL_DW, st,
+               [&] { return launch_dw(tmDz_mn, tmH_mn, s5, p5, err, std::min(s5.units, sms), st); });
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    // dH (+)= dZ_chunk W_chunk
+    Sched s6{};
+    s6.m_tiles = m_tiles_tok;
+    s6.n_tiles = d_tiles;
+    s6.k_blocks = cdiv(wc, kBK);
+    s6.group = 1;
+    s6.n_groups = d_tiles;
+    s6.units = s6.m_tiles * s6.n_groups;
+    s6.order = 1;
+    s6.b_k_off = static_cast<int>(v0);
+    EpiDhParams p6{N, Hd, dh32, static_cast<__nv_bfloat16*>(dH), c == 0, c == pl.n_chunks - 1};
+    e = launch(FLCE_KERNEL_DH, st,
+               [&] { return launch_dh(tmDz_k, tmW_mn, s6, p6, err, std::min(s6.units, sms), st); });
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return FLCE_OK;
+}
+
+const char* flce_strerror(int status) {
+  switch (status) {
+    case FLCE_OK: return "ok";
+    case FLCE_ERR_ARG: return "invalid argument (null pointer, negative size, unknown reduction or NaN)";
+    case FLCE_ERR_ALIGN: return "misaligned pointer or hidden size not a multiple of 8";
+    case FLCE_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+    case FLCE_ERR_OVERFLOW: return "sizes overflow the 64-bit byte counts or the 2^31 index limits";
+    case FLCE_ERR_CUDA: return "a CUDA runtime call failed (see flce_last_cuda_error)";
+    case FLCE_ERR_UNSUPPORTED: return "unsupported device (needs sm_103) or feature not built";
+    default: return "unknown status";
+  }
+}
+
+int flce_last_cuda_error(void) { return t_last_cuda; }
+
+uint64_t flce_launch_count(void) { return t_launches; }
+
+int flce_set_event_sink(void* const* start_events, void* const* end_events, int* kernel_ids, int capacity) {
+  if (capacity <= 0 || !start_events || !end_events || !kernel_ids) {
+    t_sink = EventSink{};
+    return 0;
+  }
+  t_sink.start = start_events;
+  t_sink.end = end_events;
+  t_sink.ids = kernel_ids;
+  t_sink.cap = capacity;
+  t_sink.used = 0;
+  return 0;
+}
+
+int flce_event_sink_used(void) { return t_sink.used; }
+
+}  // extern "C"

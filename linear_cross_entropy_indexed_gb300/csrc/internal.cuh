@@ -1,0 +1,96 @@
+// Shared definitions between the host entry points and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace flce {
+
+// Tile shape of every tensor-core kernel: 128 rows (TMEM lanes) x 256 columns
+// (fp32 TMEM columns), K staged 64 bf16 (one 128-byte swizzle row) at a time.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kATileBytes = kBM * kBK * 2;                 // 16 KiB
+constexpr int kBTileBytes = kBN * kBK * 2;                 // 32 KiB
+constexpr int kStageBytes = kATileBytes + kBTileBytes;     // 48 KiB
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;              // TMA warp, MMA warp, epilogue
+constexpr int kTmemCols = 2 * kBN;                         // double-buffered accumulator
+constexpr int kBarrierBytes = 256;
+constexpr size_t kGemmSmemBytes = 1024 + size_t(kStages) * kStageBytes + kBarrierBytes;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Persistent tile schedule.  Work is split into units; a unit is one M-tile and a run
+// of `group` consecutive N-tiles (the LSE kernel keeps a running (max, sum) across
+// them).  CTA b takes units b, b + gridDim.x, ...
+struct Sched {
+  int m_tiles;
+  int n_tiles;
+  int k_blocks;
+  int group;
+  int n_groups;
+  int units;
+  int order;     // 0: consecutive units walk M first (share the B operand); 1: walk N first
+  int b_n_off;   // added to the B operand's N coordinate (rows of W, K-major B)
+  int b_k_off;   // added to the B operand's K coordinate (rows of W, MN-major B)
+};
+
+// Per-row data the dZ epilogue needs, packed in one 16-byte load.
+struct RowInfo {
+  float lse2;    // lse * log2(e)
+  float scale;   // grad / n_valid, grad, grad_i, or 0 for an ignored row
+  int32_t label; // y_i, or -1 when the row is ignored
+  int32_t pad;
+};
+
+struct EpiLseParams {
+  int64_t N, V;
+  float softcap;        // <= 0: off
+  float* part_m;        // [n_groups][N], running max in log2 units
+  float* part_s;        // [n_groups][N], sum of 2^(z*log2e - max)
+};
+
+struct EpiDzParams {
+  int64_t N, V;
+  int64_t v0;           // first vocabulary row of this chunk
+  int64_t wc;           // chunk width (columns of dZ that exist)
+  int64_t ldz;          // row pitch of the dZ buffer in elements
+  float softcap;
+  const RowInfo* rows;
+  __nv_bfloat16* dz;
+};
+
+struct EpiDwParams {
+  int64_t rows_valid;   // chunk width: dZ^T rows that exist
+  int64_t row0;         // first output row (vocabulary index)
+  int64_t cols;         // Hd
+  __nv_bfloat16* out;   // dW, row pitch Hd
+};
+
+struct EpiDhParams {
+  int64_t N, Hd;
+  float* acc32;         // [N, Hd] fp32 running sum across vocabulary chunks
+  __nv_bfloat16* out;   // dH
+  int first, last;
+};
+
+// Launchers (defined in the kernel translation units).  Each returns the launch error.
+cudaError_t launch_linear_lse(const CUtensorMap& tmH, const CUtensorMap& tmW, const Sched& s,
+                              const EpiLseParams& p, unsigned long long* err, int grid,
+                              cudaStream_t st);
+cudaError_t launch_dz(const CUtensorMap& tmH, const CUtensorMap& tmW, const Sched& s,
+                      const EpiDzParams& p, unsigned long long* err, int grid, cudaStream_t st);
+cudaError_t launch_dw(const CUtensorMap& tmDz, const CUtensorMap& tmH, const Sched& s,
+                      const EpiDwParams& p, unsigned long long* err, int grid, cudaStream_t st);
+cudaError_t launch_dh(const CUtensorMap& tmDz, const CUtensorMap& tmW, const Sched& s,
+                      const EpiDhParams& p, unsigned long long* err, int grid, cudaStream_t st);
+cudaError_t set_gemm_smem_attributes_fwd();
+cudaError_t set_gemm_smem_attributes_bwd();
+
+}  // namespace flce

@@ -1,0 +1,179 @@
+// Memory- and latency-bound kernels of the path: label scan + indexed dot, the
+// fixed-order (max, sum) merge with the per-row loss, the final reduction, and the
+// per-row backward preparation.
+#pragma once
+
+#include "internal.cuh"
+
+namespace flce {
+
+constexpr int kDotWarps = 8;        // rows per block of the indexed-dot kernel
+constexpr int kDotMaxBlocks = 2048; // grid cap (grid-stride beyond)
+constexpr int kMergeThreads = 256;
+
+__device__ __forceinline__ float softcap_exact(float x, float c) {
+  return c > 0.0f ? c * tanhf(x / c) : x;
+}
+
+// Label scan + indexed dot: for every row i, valid_i = (y_i != ignore) && 0 <= y_i < V,
+// bad_i = (y_i != ignore) && !(0 <= y_i < V), and t_i = cap(h_i . w_{y_i}) for valid
+// rows (0 otherwise).  One warp per row, 16-byte loads, fp32 FMA, butterfly sum.
+// Per-block (n_valid, n_bad) go to blk_counts for the fixed-order final reduction.
+__global__ void __launch_bounds__(32 * kDotWarps)
+    k_label_dot(const __nv_bfloat16* __restrict__ H, const __nv_bfloat16* __restrict__ W,
+                const int64_t* __restrict__ labels, int64_t N, int64_t Hd, int64_t V, int64_t ignore,
+                float softcap, float* __restrict__ t_ws, float* __restrict__ t_user,
+                int2* __restrict__ blk_counts) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  int n_valid = 0, n_bad = 0;
+  const int64_t vec = Hd / 8;  // 16-byte vectors per row
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kDotWarps + warp; i < N;
+       i += static_cast<int64_t>(gridDim.x) * kDotWarps) {
+    const int64_t y = labels[i];
+    const bool ignored = y == ignore;
+    const bool in_range = y >= 0 && y < V;
+    const bool valid = !ignored && in_range;
+    float acc = 0.0f;
+    if (valid) {
+      const uint4* hp = reinterpret_cast<const uint4*>(H + i * Hd);
+      const uint4* wp = reinterpret_cast<const uint4*>(W + y * Hd);
+      for (int64_t k = lane; k < vec; k += 32) {
+        const uint4 a = __ldg(hp + k);
+        const uint4 b = __ldg(wp + k);
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 fa = __bfloat1622float2(a2[e]);
+          const float2 fb = __bfloat1622float2(b2[e]);
+          acc = fmaf(fa.x, fb.x, acc);
+          acc = fmaf(fa.y, fb.y, acc);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      acc = softcap_exact(acc, softcap);
+    }
+    if (lane == 0) {
+      t_ws[i] = acc;
+      if (t_user) t_user[i] = acc;
+      n_valid += valid ? 1 : 0;
+      n_bad += (!ignored && !in_range) ? 1 : 0;
+    }
+  }
+  __shared__ int sv[kDotWarps], sb[kDotWarps];
+  if (lane == 0) {
+    sv[warp] = n_valid;
+    sb[warp] = n_bad;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int a = 0, b = 0;
+    for (int w = 0; w < kDotWarps; ++w) {
+      a += sv[w];
+      b += sb[w];
+    }
+    blk_counts[blockIdx.x] = make_int2(a, b);
+  }
+}
+
+// Fixed-order merge of the per-group (max, sum) partials into lse_i, then the per-row
+// loss and a fixed-tree block sum (double) of the losses.
+__global__ void __launch_bounds__(kMergeThreads)
+    k_lse_merge(const float* __restrict__ part_m, const float* __restrict__ part_s, int n_groups,
+                int64_t N, const float* __restrict__ t, const int64_t* __restrict__ labels,
+                int64_t ignore, int64_t V, float* __restrict__ lse_out, float* __restrict__ loss_rows,
+                double* __restrict__ blk_sums) {
+  __shared__ double sh[kMergeThreads];
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kMergeThreads + threadIdx.x;
+  double mine = 0.0;
+  if (i < N) {
+    float m = -INFINITY, s = 0.0f;
+    for (int g = 0; g < n_groups; ++g) {
+      const float mg = part_m[static_cast<int64_t>(g) * N + i];
+      const float sg = part_s[static_cast<int64_t>(g) * N + i];
+      if (mg == -INFINITY) continue;  // a group that saw nothing
+      const float mn = fmaxf(m, mg);
+      s = s * exp2f(m - mn) + sg * exp2f(mg - mn);
+      m = mn;
+    }
+    const float lse = (m + log2f(s)) * kLn2;
+    lse_out[i] = lse;
+    const int64_t y = labels[i];
+    const bool valid = y != ignore && y >= 0 && y < V;
+    const float l = valid ? lse - t[i] : 0.0f;
+    if (loss_rows) loss_rows[i] = l;
+    mine = l;
+  }
+  sh[threadIdx.x] = mine;
+  __syncthreads();
+  for (int w = kMergeThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) blk_sums[blockIdx.x] = sh[0];
+}
+
+// Single block: fixed-order totals of the block sums and block counts, then the
+// reduction (mean divides once by n_valid; 0 when n_valid == 0).
+__global__ void __launch_bounds__(256)
+    k_reduce(const double* __restrict__ blk_sums, int n_sum_blocks, const int2* __restrict__ blk_counts,
+             int n_count_blocks, int reduction, float* __restrict__ loss, int64_t* __restrict__ counts) {
+  __shared__ double ss[256];
+  __shared__ long long sv[256], sb[256];
+  double s = 0.0;
+  long long v = 0, b = 0;
+  for (int k = threadIdx.x; k < n_sum_blocks; k += 256) s += blk_sums[k];
+  for (int k = threadIdx.x; k < n_count_blocks; k += 256) {
+    v += blk_counts[k].x;
+    b += blk_counts[k].y;
+  }
+  ss[threadIdx.x] = s;
+  sv[threadIdx.x] = v;
+  sb[threadIdx.x] = b;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      ss[threadIdx.x] += ss[threadIdx.x + w];
+      sv[threadIdx.x] += sv[threadIdx.x + w];
+      sb[threadIdx.x] += sb[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    counts[0] = sv[0];
+    counts[1] = sb[0];
+    if (reduction == 0) loss[0] = sv[0] > 0 ? static_cast<float>(ss[0] / static_cast<double>(sv[0])) : 0.0f;
+    if (reduction == 1) loss[0] = static_cast<float>(ss[0]);
+  }
+}
+
+// Backward per-row data: scale_i (0 for ignored rows), label (or -1), lse * log2 e.
+__global__ void k_bwd_prep(const int64_t* __restrict__ labels, const float* __restrict__ lse,
+                           const int64_t* __restrict__ counts, const float* __restrict__ grad,
+                           int reduction, int64_t N, int64_t V, int64_t ignore, RowInfo* __restrict__ out) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  const int64_t y = labels[i];
+  const bool valid = y != ignore && y >= 0 && y < V;
+  float scale = 0.0f;
+  if (valid) {
+    if (reduction == 0) {
+      const long long nv = counts[0];
+      scale = nv > 0 ? static_cast<float>(static_cast<double>(grad[0]) / static_cast<double>(nv)) : 0.0f;
+    } else if (reduction == 1) {
+      scale = grad[0];
+    } else {
+      scale = grad[i];
+    }
+  }
+  RowInfo r;
+  r.lse2 = lse[i] * kLog2e;
+  r.scale = scale;
+  r.label = valid ? static_cast<int32_t>(y) : -1;
+  r.pad = 0;
+  out[i] = r;
+}
+
+}  // namespace flce

@@ -1,0 +1,451 @@
+// Persistent, warp-specialised tcgen05 GEMM engine with pluggable epilogues.
+//
+//   warp 0      TMA producer: stages A (128 x 64) and B (256 x 64) bf16 tiles into a
+//               4-deep shared-memory ring, 128-byte swizzled.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256, K=16) into
+//               one of two TMEM accumulators (2 x 256 fp32 columns) and commits to
+//               mbarriers that free ring slots / publish finished accumulators.
+//   warps 2..5  epilogue: each warp owns the 32 TMEM lanes (rows) of its lane
+//               quadrant, pulls 32 columns at a time with tcgen05.ld and runs the
+//               epilogue (online LSE, dZ, dW store, dH accumulate) while the MMA warp
+//               already fills the other accumulator.
+//
+// Operands are K-major ([rows, K] with K contiguous) or MN-major ([K, rows] with rows
+// contiguous); both use the 128-byte swizzle that the TMA writes:
+//   K-major : one box {64 K, R rows};    8-row groups 1024 B apart (SBO), K step = +32 B
+//   MN-major: R/64 boxes {64 rows, 64 K}; 64-row atoms 8 KiB apart (LBO), 8-K groups
+//             1024 B apart (SBO), K step of 16 = +2 KiB
+#pragma once
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace flce {
+
+__device__ __forceinline__ void decode_unit(const Sched& s, int u, int& mt, int& g) {
+  if (s.order == 0) {
+    g = u / s.m_tiles;
+    mt = u - g * s.m_tiles;
+  } else {
+    mt = u / s.n_groups;
+    g = u - mt * s.n_groups;
+  }
+}
+
+template <bool MN, int ROWS>
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* tm, uint32_t bar,
+                                             int row0, int k0) {
+  if constexpr (!MN) {
+    tma_load_2d(dst, tm, bar, k0, row0);
+  } else {
+#pragma unroll
+    for (int j = 0; j < ROWS / 64; ++j) tma_load_2d(dst + j * 8192, tm, bar, row0 + j * 64, k0);
+  }
+}
+
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int k) {
+  if constexpr (!MN) {
+    return smem_desc_sw128(base + k * 32, 16, 1024);
+  } else {
+    return smem_desc_sw128(base + k * 2048, 8192, 1024);
+  }
+}
+
+template <class Epi, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const Sched sched, const typename Epi::Params ep, unsigned long long* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  // bars: full[kStages], empty[kStages], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t tiles_u32 = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kStages;
+  const uint32_t tfull0 = empty0 + 8 * kStages;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, kEpiWarps * 32);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0;  // bit s: stage s armed at least once; parity of last arm below
+      uint32_t armed_parity = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+        int mt, g;
+        decode_unit(sched, u, mt, g);
+        const int nt0 = g * sched.group;
+        const int nt1 = min(nt0 + sched.group, sched.n_tiles);
+        for (int nt = nt0; ok && nt < nt1; ++nt) {
+          for (int kb = 0; kb < sched.k_blocks; ++kb) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = full0 + 8 * stage;
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            const uint32_t a = tiles_u32 + stage * kStageBytes;
+            load_operand<A_MN, kBM>(a, &tmA, fb, mt * kBM, kb * kBK);
+            load_operand<B_MN, kBN>(a + kATileBytes, &tmB, fb, nt * kBN + sched.b_n_off,
+                                    kb * kBK + sched.b_k_off);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Let loads already in flight land before the CTA's shared memory goes away.
+        volatile int never = 0;
+        for (int s = 0; s < kStages; ++s)
+          if (armed & (1u << s)) mbar_wait(full0 + 8 * s, (armed_parity >> s) & 1u, &never, err);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+        int mt, g;
+        decode_unit(sched, u, mt, g);
+        const int nt0 = g * sched.group;
+        const int nt1 = min(nt0 + sched.group, sched.n_tiles);
+        for (int nt = nt0; ok && nt < nt1; ++nt) {
+          if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + acc * kBN;
+          for (int kb = 0; kb < sched.k_blocks; ++kb) {
+            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a = tiles_u32 + stage * kStageBytes;
+            const uint32_t b = a + kATileBytes;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_bf16(d, operand_desc<A_MN>(a, k), operand_desc<B_MN>(b, k), idesc,
+                       (kb | k) != 0 ? 1u : 0u);
+            issued = true;
+            mma_commit(empty0 + 8 * stage);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          mma_commit(tfull0 + 8 * acc);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1;
+          }
+        }
+      }
+      if (!ok && issued) {
+        // Wait (bounded) for every MMA this thread issued before TMEM is released.
+        volatile int never = 0;
+        mma_commit(drain);
+        mbar_wait(drain, 0, &never, err);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+      int mt, g;
+      decode_unit(sched, u, mt, g);
+      const int nt0 = g * sched.group;
+      const int nt1 = min(nt0 + sched.group, sched.n_tiles);
+      const int64_t row = static_cast<int64_t>(mt) * kBM + row_in_tile;
+      typename Epi::State st;
+      Epi::unit_begin(ep, st);
+      for (int nt = nt0; nt < nt1; ++nt) {
+        if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
+        Epi::tile(ep, st, taddr, row, nt);
+        tc_fence_before();
+        mbar_arrive(tempty0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      Epi::unit_end(ep, st, row, g);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ====================================================================== epilogues
+// Tanh softcap from exp2: tanh(u) = 1 - 2 / (e^{2u} + 1), with e^{2u} = 2^{2u log2 e}.
+// Absolute error of the result is a few fp32 ulps of 1 (no cancellation blow-up for
+// small u, saturates to +-1 for large |u|).
+__device__ __forceinline__ float tanh_via_exp2(float u) {
+  const float e = ex2_approx(u * (2.0f * kLog2e));
+  return 1.0f - 2.0f * rcp_approx(e + 1.0f);
+}
+
+// Forward: running (max, sum) of 2^(z log2 e) over the unit's vocabulary tiles.
+struct EpiLse {
+  using Params = EpiLseParams;
+  struct State {
+    float m;  // running max of z*log2e
+    float s;  // sum of 2^(z*log2e - m)
+  };
+  __device__ static void unit_begin(const Params&, State& st) {
+    st.m = -INFINITY;
+    st.s = 0.0f;
+  }
+  __device__ static void tile(const Params& p, State& st, uint32_t taddr, int64_t, int nt) {
+    const int64_t v_base = static_cast<int64_t>(nt) * kBN;
+    const bool tail = v_base + kBN > p.V;
+    const bool cap = p.softcap > 0.0f;
+    const float inv_c = cap ? 1.0f / p.softcap : 0.0f;
+    const float c_log2e = p.softcap * kLog2e;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      float x[32];
+      __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
+      tmem_ld32(taddr + c * 32, x);
+      float cmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float z = cap ? c_log2e * tanh_via_exp2(x[j] * inv_c) : x[j] * kLog2e;
+        if (tail && v_base + c * 32 + j >= p.V) z = -INFINITY;
+        x[j] = z;
+        cmax = fmaxf(cmax, z);
+      }
+      if (cmax == -INFINITY) continue;  // the whole 32-column slice is past V
+      const float mn = fmaxf(st.m, cmax);
+      float acc = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc += ex2_approx(x[j] - mn);
+      st.s = st.s * ex2_approx(st.m - mn) + acc;  // 2^-inf = 0 for the first slice
+      st.m = mn;
+    }
+  }
+  __device__ static void unit_end(const Params& p, State& st, int64_t row, int g) {
+    if (row < p.N) {
+      p.part_m[static_cast<int64_t>(g) * p.N + row] = st.m;
+      p.part_s[static_cast<int64_t>(g) * p.N + row] = st.s;
+    }
+  }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Backward: recompute the logit tile, dZ = (p - onehot) * scale * cap', bf16 store.
+struct EpiDz {
+  using Params = EpiDzParams;
+  struct State {};
+  __device__ static void unit_begin(const Params&, State&) {}
+  __device__ static void unit_end(const Params&, State&, int64_t, int) {}
+  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt) {
+    RowInfo ri{0.0f, 0.0f, -1, 0};
+    const bool row_ok = row < p.N;
+    if (row_ok) ri = p.rows[row];
+    const bool cap = p.softcap > 0.0f;
+    const float inv_c = cap ? 1.0f / p.softcap : 0.0f;
+    const float c_log2e = p.softcap * kLog2e;
+    const int64_t vl_tile = static_cast<int64_t>(nt) * kBN;
+    const int64_t y_local = ri.label >= 0 ? static_cast<int64_t>(ri.label) - p.v0 : -1;
+    __nv_bfloat16* out_row = p.dz + (row_ok ? row : 0) * p.ldz;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      float x[32];
+      __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
+      tmem_ld32(taddr + c * 32, x);
+      const int64_t vl = vl_tile + c * 32;
+      if (!row_ok || vl >= p.wc) continue;
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        float d[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float xv = x[j + h];
+          float z2, dcap;
+          if (cap) {
+            const float t = tanh_via_exp2(xv * inv_c);
+            z2 = c_log2e * t;
+            dcap = 1.0f - t * t;
+          } else {
+            z2 = xv * kLog2e;
+            dcap = 1.0f;
+          }
+          float g = ex2_approx(z2 - ri.lse2);
+          if (vl + j + h == y_local) g -= 1.0f;
+          d[h] = g * ri.scale * dcap;
+        }
+        pk[j / 2] = pack_bf16x2(d[0], d[1]);
+      }
+      if (vl + 32 <= p.wc) {
+        uint4* dst = reinterpret_cast<uint4*>(out_row + vl);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+      } else {
+        for (int j = 0; j < 32 && vl + j < p.wc; ++j) {
+          const uint32_t w = pk[j / 2];
+          const uint16_t hbits = static_cast<uint16_t>((j & 1) ? (w >> 16) : (w & 0xFFFFu));
+          reinterpret_cast<uint16_t*>(out_row)[vl + j] = hbits;
+        }
+      }
+    }
+  }
+};
+
+// Backward: dW chunk = dZ^T H, converted to bf16 and written once.
+struct EpiDw {
+  using Params = EpiDwParams;
+  struct State {};
+  __device__ static void unit_begin(const Params&, State&) {}
+  __device__ static void unit_end(const Params&, State&, int64_t, int) {}
+  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt) {
+    const bool row_ok = row < p.rows_valid;
+    __nv_bfloat16* out_row = p.out + (p.row0 + (row_ok ? row : 0)) * p.cols;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      float x[32];
+      __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
+      tmem_ld32(taddr + c * 32, x);
+      const int64_t col = static_cast<int64_t>(nt) * kBN + c * 32;
+      if (!row_ok || col >= p.cols) continue;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (col + 8 * k + 8 <= p.cols) {
+          uint4 v = make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
+                               pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
+          *reinterpret_cast<uint4*>(out_row + col + 8 * k) = v;
+        }
+      }
+    }
+  }
+};
+
+// Backward: dH += dZ_chunk W_chunk; fp32 running sum across chunks, bf16 at the end.
+struct EpiDh {
+  using Params = EpiDhParams;
+  struct State {};
+  __device__ static void unit_begin(const Params&, State&) {}
+  __device__ static void unit_end(const Params&, State&, int64_t, int) {}
+  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt) {
+    const bool row_ok = row < p.N;
+    const int64_t base = (row_ok ? row : 0) * p.Hd;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      float x[32];
+      __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
+      tmem_ld32(taddr + c * 32, x);
+      const int64_t col = static_cast<int64_t>(nt) * kBN + c * 32;
+      if (!row_ok || col >= p.Hd) continue;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t cc = col + 8 * k;
+        if (cc + 8 > p.Hd) continue;
+        float* a = p.acc32 + base + cc;
+        if (!p.first) {
+          const float4 u0 = *reinterpret_cast<const float4*>(a);
+          const float4 u1 = *reinterpret_cast<const float4*>(a + 4);
+          x[8 * k + 0] += u0.x;
+          x[8 * k + 1] += u0.y;
+          x[8 * k + 2] += u0.z;
+          x[8 * k + 3] += u0.w;
+          x[8 * k + 4] += u1.x;
+          x[8 * k + 5] += u1.y;
+          x[8 * k + 6] += u1.z;
+          x[8 * k + 7] += u1.w;
+        }
+        if (p.last) {
+          uint4 v = make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
+                               pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
+          *reinterpret_cast<uint4*>(p.out + base + cc) = v;
+        } else {
+          *reinterpret_cast<float4*>(a) = make_float4(x[8 * k], x[8 * k + 1], x[8 * k + 2], x[8 * k + 3]);
+          *reinterpret_cast<float4*>(a + 4) = make_float4(x[8 * k + 4], x[8 * k + 5], x[8 * k + 6], x[8 * k + 7]);
+        }
+      }
+    }
+  }
+};
+
+template <class Epi, bool A_MN, bool B_MN>
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Sched& s,
+                        const typename Epi::Params& p, unsigned long long* err, int grid,
+                        cudaStream_t st) {
+  tc_gemm_kernel<Epi, A_MN, B_MN><<<grid, kThreads, kGemmSmemBytes, st>>>(tmA, tmB, s, p, err);
+  return cudaGetLastError();
+}
+
+template <class Epi, bool A_MN, bool B_MN>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(tc_gemm_kernel<Epi, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kGemmSmemBytes));
+}
+
+}  // namespace flce

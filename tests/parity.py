@@ -1,0 +1,114 @@
+"""Shared helpers of the GPU parity tests: seeded inputs, the CUDA path through the
+C ABI (via the binding), and comparisons with the fp64 oracle.
+
+Tolerances (fp32 accumulation of bf16 products, bf16 gradient outputs):
+  loss      relative error <= 1e-3
+  lse       absolute error <= 2e-3 per row
+  target    absolute error <= 1e-3 per valid row (the indexed-dot output)
+  dH, dW    relative Frobenius error <= 1e-2
+  counts    bit-exact
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+import synthetic as S
+
+TOL_LOSS_REL = 1e-3
+TOL_LSE_ABS = 2e-3
+TOL_TARGET_ABS = 1e-3
+TOL_GRAD_FRO = 1e-2
+
+
+def to_device(bits: np.ndarray, dev="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def fro_rel(a: np.ndarray, ref: np.ndarray) -> float:
+    num = np.linalg.norm((a - ref).ravel())
+    den = np.linalg.norm(ref.ravel())
+    return float(num / den) if den > 0 else float(num)
+
+
+def make_case(w: S.Workload, labels: np.ndarray | None = None):
+    Hb = S.make_H(w)
+    Wb = S.make_W(w)
+    y = S.make_labels(w) if labels is None else labels
+    return Hb, Wb, y
+
+
+def run_gpu(Hb, Wb, y, ignore_index=-100, softcap=0.0, reduction="mean", grad=None, chunk_budget=0,
+            backward=True):
+    import linear_cross_entropy_indexed_gb300 as F
+    H = to_device(Hb)
+    W = to_device(Wb)
+    lab = torch.from_numpy(np.asarray(y, dtype=np.int64)).cuda()
+    loss, lse, counts, tgt = F.flce_forward(H, W, lab, ignore_index, softcap, reduction, want_target=True)
+    out = dict(loss=loss.double().cpu().numpy(), lse=lse.double().cpu().numpy(), counts=counts.cpu().numpy(),
+               target=tgt.double().cpu().numpy())
+    if backward:
+        N = H.shape[0]
+        if grad is None:
+            grad = np.linspace(0.5, 1.5, N) if reduction == "none" else np.array([1.0])
+        g = torch.tensor(np.asarray(grad, dtype=np.float32)).cuda()
+        dH, dW = F.flce_backward(H, W, lab, lse, counts, g, ignore_index, softcap, reduction, chunk_budget)
+        out["dH"] = S.bf16_bits_to_f32(bf16_bits(dH)).astype(np.float64)
+        out["dW"] = S.bf16_bits_to_f32(bf16_bits(dW)).astype(np.float64)
+        out["counts_after"] = counts.cpu().numpy()
+    torch.cuda.synchronize()
+    return out
+
+
+def check_forward(out, ref: O.Forward, y, V, ignore_index=-100, reduction="mean"):
+    valid, bad = O.label_status(y, V, ignore_index)
+    assert int(out["counts"][0]) == ref.n_valid, (out["counts"], ref.n_valid)
+    assert int(out["counts"][1]) == ref.n_bad
+    assert int(out["counts"][2]) == 0, "device error bits set"
+    lse_err = np.abs(out["lse"] - ref.lse).max() if len(ref.lse) else 0.0
+    assert lse_err <= TOL_LSE_ABS, "lse abs err %g" % lse_err
+    t_err = np.abs(out["target"] - ref.target)[valid].max() if valid.any() else 0.0
+    assert t_err <= TOL_TARGET_ABS, "target abs err %g" % t_err
+    assert np.all(out["target"][~valid] == 0)
+    if reduction == "none":
+        ref_l = np.asarray(ref.loss)
+        err = np.abs(out["loss"] - ref_l).max() if len(ref_l) else 0.0
+        assert err <= TOL_LSE_ABS + TOL_TARGET_ABS, "per-row loss err %g" % err
+        assert np.all(out["loss"][~valid] == 0)
+    else:
+        ref_l = float(ref.loss)
+        got = float(out["loss"])
+        if ref_l == 0.0:
+            assert got == 0.0
+        else:
+            assert abs(got - ref_l) / abs(ref_l) <= TOL_LOSS_REL, (got, ref_l)
+    return dict(lse_err=float(lse_err), target_err=float(t_err))
+
+
+def check_backward(out, dH_ref, dW_ref):
+    eh = fro_rel(out["dH"], dH_ref)
+    ew = fro_rel(out["dW"], dW_ref)
+    assert np.isfinite(out["dH"]).all() and np.isfinite(out["dW"]).all()
+    assert eh <= TOL_GRAD_FRO, "dH rel fro err %g" % eh
+    assert ew <= TOL_GRAD_FRO, "dW rel fro err %g" % ew
+    assert int(out["counts_after"][2]) == 0, "device error bits set"
+    return dict(dH_err=eh, dW_err=ew)
+
+
+def oracle_full(Hb, Wb, y, ignore_index=-100, softcap=0.0, reduction="mean", grad=None):
+    Hf = O.widen_bf16(Hb)
+    Wf = O.widen_bf16(Wb)
+    ref = O.forward(Hf, Wf, y, ignore_index, softcap, reduction)
+    N = Hf.shape[0]
+    if grad is None:
+        grad = np.linspace(0.5, 1.5, N) if reduction == "none" else 1.0
+    g = np.asarray(grad, dtype=np.float32).astype(np.float64)
+    if reduction != "none":
+        g = float(np.asarray(g).reshape(-1)[0])
+    dH, dW = O.backward(Hf, Wf, y, ref.lse, ignore_index, softcap, reduction, g)
+    return ref, dH, dW

@@ -1,0 +1,114 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every symbol
+declared in include/flce.h, sizes the workspace, and rejects bad arguments with a
+status before it touches the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_cross_entropy_indexed_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flce.h")
+
+OK, ARG, ALIGN, WS, OVERFLOW, CUDA, UNSUP = range(7)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = _build.build()
+    import linear_cross_entropy_indexed_gb300 as F
+    return F.library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"FLCE_API\s+[\w\s\*]+?\b(flce_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ("flce_forward", "flce_backward", "flce_forward_workspace_size", "flce_backward_workspace_size",
+              "flce_strerror"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_symbols():
+        assert hasattr(lib, n), n
+    nm = os.popen("nm -D --defined-only %s" % _build.LIB).read()
+    exported = set(re.findall(r"\bT (flce_\w+)", nm))
+    assert set(declared_symbols()) <= exported
+
+
+def test_strerror(lib):
+    for s in range(7):
+        assert lib.flce_strerror(s)
+    assert b"unknown" in lib.flce_strerror(99)
+
+
+def test_workspace_sizes(lib):
+    f = lib.flce_forward_workspace_size
+    b = lib.flce_backward_workspace_size
+    assert f(256, 64, 2000) > 0
+    assert f(0, 64, 2000) > 0 or f(0, 64, 2000) == 0
+    assert f(-1, 64, 2000) == 0 and f(8, 63, 100) == 0 and f(8, 64, 0) == 0
+    # forward scratch is O(N * V / 1024) (one (max, sum) pair per row per 1024-column group)
+    n, hd, v = 8192, 4096, 128256
+    groups = -(-(-(-v // 256)) // 4)
+    assert f(n, hd, v) >= 2 * groups * n * 4
+    assert f(n, hd, v) < 2 * groups * n * 4 + (1 << 20)
+    # backward: one bf16 [N, Vc] chunk plus an fp32 [N, Hd] accumulator when chunked
+    budget = 64 << 20
+    vc = (budget // (2 * n)) // 256 * 256
+    size = b(n, hd, v, budget)
+    assert size >= n * vc * 2 + n * hd * 4 + n * 16
+    assert size < n * vc * 2 + n * hd * 4 + n * 16 + (1 << 12)
+    # a single chunk needs no fp32 accumulator
+    assert b(256, 64, 2000, 0) < 256 * 2048 * 2 + 256 * 16 + 4096
+
+
+def _fwd(lib, H=0x1000, W=0x2000, labels=0x3000, N=16, Hd=64, V=100, red=0, loss=0x4000, lse=0x5000,
+         counts=0x6000, ws=0x10000, ws_bytes=1 << 20, softcap=0.0):
+    return lib.flce_forward(H, W, labels, N, Hd, V, -100, softcap, red, loss, lse, None, counts, ws, ws_bytes, None)
+
+
+def _bwd(lib, N=16, Hd=64, V=100, red=0, filt=0.0, ws_bytes=1 << 24, dW=0x7000, W=0x2000):
+    return lib.flce_backward(0x1000, W, 0x3000, 0x5000, 0x6000, N, Hd, V, -100, 0.0, red, 0x8000, filt, 0x9000,
+                             dW, 0x10000, ws_bytes, 0, None)
+
+
+def test_argument_errors_before_any_device_work(lib):
+    assert _fwd(lib, H=None) == ARG
+    assert _fwd(lib, W=None) == ARG
+    assert _fwd(lib, red=3) == ARG
+    assert _fwd(lib, N=-1) == ARG
+    assert _fwd(lib, V=0) == ARG
+    assert _fwd(lib, softcap=float("nan")) == ARG
+    assert _fwd(lib, Hd=60) == ALIGN
+    assert _fwd(lib, H=0x1008) == ALIGN
+    assert _fwd(lib, W=0x2004) == ALIGN
+    assert _fwd(lib, ws_bytes=16) == WS
+    assert _fwd(lib, ws=0x10010) == WS
+    assert _fwd(lib, N=1 << 40) == OVERFLOW
+    assert _bwd(lib, filt=0.5) == UNSUP
+    assert _bwd(lib, dW=None) == ARG
+    assert _bwd(lib, ws_bytes=16) == WS
+    assert _bwd(lib, W=0x2002) == ALIGN
+
+
+def test_valid_arguments_without_a_device_fail_cleanly(lib):
+    # Arguments pass the checks; without a GPU the first CUDA call fails and the
+    # library reports FLCE_ERR_CUDA (nothing is dereferenced on the host).
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert _fwd(lib) == CUDA
+    assert lib.flce_last_cuda_error() != 0
+
+
+def test_event_sink_toggles(lib):
+    lib.flce_set_event_sink(None, None, None, 0)
+    assert lib.flce_event_sink_used() == 0
+    assert lib.flce_launch_count() >= 0
