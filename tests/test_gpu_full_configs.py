@@ -1,0 +1,66 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py times
+(default vocabulary chunk budget).
+
+For each workload the fp64 oracle computes every row's LSE (row blocks, library
+matmul), so lse, the target logits and the mean loss are compared for all rows.  dH
+is compared on 96 sampled rows and dW on 160 sampled vocabulary rows (the 48 most
+frequent labels, 64 uniform ids, the last 48 ids including the ragged last tile);
+their relative Frobenius errors are estimated on those samples."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic as S
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample_vocab(y, V, rng):
+    yv = y[y >= 0]
+    freq = np.bincount(yv, minlength=V)
+    top = np.argsort(-freq, kind="stable")[:48]
+    uni = rng.choice(V, 64, replace=False)
+    last = np.arange(V - 48, V)
+    return np.unique(np.concatenate([top, uni, last]))
+
+
+@pytest.mark.parametrize("name", ["llama2", "llama3", "gemma2", "packed"])
+def test_full_size_workload(name):
+    import linear_cross_entropy_indexed_gb300 as F
+    w = S.WORKLOADS[name]
+    Hb, Wb, y = S.make_H(w), S.make_W(w), S.make_labels(w)
+    H, W = P.to_device(Hb), P.to_device(Wb)
+    lab = torch.from_numpy(y).cuda()
+    loss, lse, counts, tgt = F.flce_forward(H, W, lab, w.ignore_index, w.softcap, w.reduction, want_target=True)
+    g = torch.ones(1, device="cuda")
+    dH, dW = F.flce_backward(H, W, lab, lse, counts, g, w.ignore_index, w.softcap, w.reduction)
+    torch.cuda.synchronize()
+    got_lse = lse.double().cpu().numpy()
+    got_t = tgt.double().cpu().numpy()
+    c = counts.cpu().numpy()
+    del H, W
+
+    Hf, Wf = O.widen_bf16(Hb), O.widen_bf16(Wb)
+    ref = O.forward(Hf, Wf, y, w.ignore_index, w.softcap, w.reduction, row_block=1024)
+    valid, bad = O.label_status(y, w.V, w.ignore_index)
+    assert int(c[0]) == ref.n_valid and int(c[1]) == ref.n_bad and int(c[2]) == 0
+    assert np.abs(got_lse - ref.lse).max() <= P.TOL_LSE_ABS
+    assert np.abs(got_t - ref.target)[valid].max() <= P.TOL_TARGET_ABS
+    assert abs(float(loss) - float(ref.loss)) / float(ref.loss) <= P.TOL_LOSS_REL
+
+    rng = np.random.default_rng(1000 + w.seed)
+    rows = np.unique(np.concatenate([[0, w.N - 1], rng.choice(w.N, 94, replace=False)]))
+    dh_ref = O.dH_rows(Hf, Wf, y, ref.lse[rows], rows, w.ignore_index, w.softcap, w.reduction, 1.0,
+                       n_valid=ref.n_valid)
+    dh_got = S.bf16_bits_to_f32(P.bf16_bits(dH[torch.from_numpy(rows).cuda()])).astype(np.float64)
+    assert P.fro_rel(dh_got, dh_ref) <= P.TOL_GRAD_FRO
+    vs = _sample_vocab(y, w.V, rng)
+    dw_ref = O.dW_rows(Hf, Wf, y, ref.lse, vs, w.ignore_index, w.softcap, w.reduction, 1.0)
+    dw_got = S.bf16_bits_to_f32(P.bf16_bits(dW[torch.from_numpy(vs).cuda()])).astype(np.float64)
+    assert P.fro_rel(dw_got, dw_ref) <= P.TOL_GRAD_FRO
+    # ignored rows carry no gradient
+    ign = np.nonzero(~valid)[0][:16]
+    if len(ign):
+        assert dH[torch.from_numpy(ign).cuda()].abs().max().item() == 0.0
