@@ -128,6 +128,32 @@ FLCE_API flce_status flce_backward(const void* H, const void* W, const int64_t* 
                           void* workspace, size_t workspace_bytes, size_t chunk_budget_bytes,
                           void* stream);
 
+/* Forward pass that allocates nothing and takes no workspace.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate device memory
+ * where they compute the loss (a plug-in inside a runtime that owns all device memory
+ * through its own pool, a process that reserves its memory once at start-up, a path
+ * that cannot afford an allocation's implicit synchronisation).
+ * Arguments and outputs are those of flce_forward without workspace/workspace_bytes.
+ * The forward's scratch is one static device array inside the library of
+ * flce_static_scratch_bytes() bytes (16 MiB); every GPU that loads the library holds it
+ * until the process exits.
+ *   - Returns FLCE_ERR_WORKSPACE, before enqueuing anything, when
+ *     flce_forward_workspace_size(N, Hd, V) exceeds that size (N = 8192 fits V up to
+ *     about 256K; larger problems must use flce_forward with their own workspace).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call before
+ *     any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents.  Nothing
+ *     in it has to start at zero: each call writes every scratch word before reading
+ *     it.  Calls that overlap on the GPU (on two streams, or from two host threads)
+ *     race on the array and must be serialised by the caller. */
+FLCE_API size_t flce_static_scratch_bytes(void);
+FLCE_API flce_status flce_forward_noalloc(const void* H, const void* W, const int64_t* labels,
+                                 int64_t N, int64_t Hd, int64_t V, int64_t ignore_index,
+                                 float softcap, int reduction,
+                                 float* loss, float* lse, float* target_logit, int64_t* counts,
+                                 void* stream);
+
 /* Human-readable text for a flce_status value. */
 FLCE_API const char* flce_strerror(int status);
 

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libflce.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["flce_api.cu", "gemm_fwd.cu", "gemm_bwd.cu"]
+SOURCES = ["flce_api.cu", "gemm_fwd.cu", "gemm_bwd.cu", "flce_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,77 @@
+// Forward pass that allocates nothing and needs no caller-provided workspace.
+//
+// Who needs this: callers that cannot call cudaMalloc (or any allocator) at the point
+// where they compute the loss — for example a C plug-in inside another runtime that
+// owns all device memory through its own pool and forbids further driver allocations,
+// a serving process that reserves its memory once at start-up, or a latency-critical
+// path where an allocation's implicit synchronisation is not acceptable.  They still
+// pass their own inputs and outputs; only the forward's scratch comes from here.
+//
+// The scratch is one file-scope __device__ array of kStaticScratchBytes.  Every GPU
+// that loads this library holds that much memory until the process exits.  In host
+// code the array's name is only a host-side stand-in, so the device address is looked
+// up once per device with cudaGetSymbolAddress (with that device current) and passed
+// to the kernels like any workspace pointer.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "flce.h"
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+struct ScratchAddress {
+  bool looked_up = false;
+  cudaError_t err = cudaSuccess;
+  void* ptr = nullptr;
+};
+ScratchAddress g_scratch[kMaxDevices];
+std::mutex g_scratch_mu;
+
+// Device address of the static scratch on the current device (looked up on the
+// first call per device).
+flce_status static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FLCE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  ScratchAddress& s = g_scratch[dev];
+  if (!s.looked_up) {
+    void* p = nullptr;
+    s.err = cudaGetSymbolAddress(&p, g_static_scratch);
+    s.ptr = s.err == cudaSuccess ? p : nullptr;
+    s.looked_up = true;
+  }
+  if (s.err != cudaSuccess || s.ptr == nullptr) return FLCE_ERR_CUDA;
+  *out = s.ptr;
+  return FLCE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+FLCE_API size_t flce_static_scratch_bytes(void) { return kStaticScratchBytes; }
+
+FLCE_API flce_status flce_forward_noalloc(const void* H, const void* W, const int64_t* labels, int64_t N,
+                                          int64_t Hd, int64_t V, int64_t ignore_index, float softcap,
+                                          int reduction, float* loss, float* lse, float* target_logit,
+                                          int64_t* counts, void* stream) {
+  const size_t need = flce_forward_workspace_size(N, Hd, V);
+  if (need > kStaticScratchBytes) return FLCE_ERR_WORKSPACE;  // sizes beyond the static scratch
+  void* scratch = nullptr;
+  if (need > 0) {
+    const flce_status s = static_scratch(&scratch);
+    if (s != FLCE_OK) return s;
+  }
+  // need == 0 means invalid sizes (or nothing to do); flce_forward reports which.
+  return flce_forward(H, W, labels, N, Hd, V, ignore_index, softcap, reduction, loss, lse, target_logit, counts,
+                      scratch, kStaticScratchBytes, stream);
+}
+
+}  // extern "C"
