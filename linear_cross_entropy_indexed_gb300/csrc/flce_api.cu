@@ -123,6 +123,9 @@ bool tmap_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, 
 
 int cdiv(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
+// CTA pairs run one 256-row tile each: an even grid of at most one CTA per SM.
+int pair_grid(int units, int sms) { return 2 * std::max(1, std::min(units, sms / 2)); }
+
 // ------------------------------------------------------------------ planning
 struct FwdPlan {
   int m_tiles = 0, v_tiles = 0, n_groups = 0, k_blocks = 0;
@@ -145,7 +148,7 @@ flce_status check_sizes(int64_t N, int64_t Hd, int64_t V) {
 flce_status plan_forward(int64_t N, int64_t Hd, int64_t V, FwdPlan* p) {
   flce_status s = check_sizes(N, Hd, V);
   if (s != FLCE_OK) return s;
-  p->m_tiles = cdiv(N, kBM);
+  p->m_tiles = cdiv(N, kPairM);  // CTA pairs: 256 token rows per tile
   p->v_tiles = cdiv(V, kBN);
   p->n_groups = cdiv(p->v_tiles, kLseGroup);
   p->k_blocks = cdiv(Hd, kBK);
@@ -252,7 +255,7 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* labels, in
 
   // (2) tensor-core linear-LSE
   CUtensorMap tmH, tmW;
-  if (!tmap_2d(&tmH, H, Hd, N, Hd * 2, kBK, kBM) || !tmap_2d(&tmW, W, Hd, V, Hd * 2, kBK, kBN))
+  if (!tmap_2d(&tmH, H, Hd, N, Hd * 2, kBK, kBM) || !tmap_2d(&tmW, W, Hd, V, Hd * 2, kBK, kBN / 2))
     return FLCE_ERR_CUDA;
   Sched sc{};
   sc.m_tiles = pl.m_tiles;
@@ -263,7 +266,7 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* labels, in
   sc.units = pl.m_tiles * pl.n_groups;
   sc.order = 0;
   EpiLseParams lp{N, V, softcap, part_m, part_s};
-  const int grid = std::min(sc.units, sms);
+  const int grid = pair_grid(sc.units, sms);
   e = launch(FLCE_KERNEL_LINEAR_LSE, st, [&] { return launch_linear_lse(tmH, tmW, sc, lp, err, grid, st); });
   if (e != cudaSuccess) return cuda_fail(e);
 
@@ -324,11 +327,11 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
   if (e != cudaSuccess) return cuda_fail(e);
 
   CUtensorMap tmH_k, tmW_k, tmH_mn, tmW_mn;
-  if (!tmap_2d(&tmH_k, H, Hd, N, Hd * 2, kBK, kBM) || !tmap_2d(&tmW_k, W, Hd, V, Hd * 2, kBK, kBN) ||
+  if (!tmap_2d(&tmH_k, H, Hd, N, Hd * 2, kBK, kBM) || !tmap_2d(&tmW_k, W, Hd, V, Hd * 2, kBK, kBN / 2) ||
       !tmap_2d(&tmH_mn, H, Hd, N, Hd * 2, 64, kBK) || !tmap_2d(&tmW_mn, W, Hd, V, Hd * 2, 64, kBK))
     return FLCE_ERR_CUDA;
 
-  const int m_tiles_tok = cdiv(N, kBM);
+  const int m_tiles_tok = cdiv(N, kPairM);
   const int d_tiles = cdiv(Hd, kBN);
   for (int c = 0; c < pl.n_chunks; ++c) {
     const int64_t v0 = int64_t(c) * pl.Vc;
@@ -349,12 +352,12 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
     s4.b_n_off = static_cast<int>(v0);
     EpiDzParams p4{N, V, v0, wc, pl.Vc, softcap, rows, dz};
     e = launch(FLCE_KERNEL_DZ, st,
-               [&] { return launch_dz(tmH_k, tmW_k, s4, p4, err, std::min(s4.units, sms), st); });
+               [&] { return launch_dz(tmH_k, tmW_k, s4, p4, err, pair_grid(s4.units, sms), st); });
     if (e != cudaSuccess) return cuda_fail(e);
 
     // dW rows [v0, v0 + wc) = dZ_chunk^T H
     Sched s5{};
-    s5.m_tiles = cdiv(wc, kBM);
+    s5.m_tiles = cdiv(wc, kPairM);
     s5.n_tiles = d_tiles;
     s5.k_blocks = cdiv(N, kBK);
     s5.group = 1;
@@ -363,7 +366,7 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
     s5.order = 1;
     EpiDwParams p5{wc, v0, Hd, static_cast<__nv_bfloat16*>(dW)};
     e = launch(FLCE_KERNEL_DW, st,
-               [&] { return launch_dw(tmDz_mn, tmH_mn, s5, p5, err, std::min(s5.units, sms), st); });
+               [&] { return launch_dw(tmDz_mn, tmH_mn, s5, p5, err, pair_grid(s5.units, sms), st); });
     if (e != cudaSuccess) return cuda_fail(e);
 
     // dH (+)= dZ_chunk W_chunk
@@ -378,7 +381,7 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
     s6.b_k_off = static_cast<int>(v0);
     EpiDhParams p6{N, Hd, dh32, static_cast<__nv_bfloat16*>(dH), c == 0, c == pl.n_chunks - 1};
     e = launch(FLCE_KERNEL_DH, st,
-               [&] { return launch_dh(tmDz_k, tmW_mn, s6, p6, err, std::min(s6.units, sms), st); });
+               [&] { return launch_dh(tmDz_k, tmW_mn, s6, p6, err, pair_grid(s6.units, sms), st); });
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return FLCE_OK;

@@ -8,27 +8,29 @@
 
 namespace flce {
 
-// Tile shape of every tensor-core kernel: 128 rows (TMEM lanes) x 256 columns
-// (fp32 TMEM columns), K staged 64 bf16 (one 128-byte swizzle row) at a time.
-constexpr int kBM = 128;
-constexpr int kBN = 256;
+// Tile shape of every tensor-core kernel: a CTA pair computes 256 x 256 fp32 tiles;
+// each CTA owns 128 of the rows (its TMEM lanes) and stages K 64 bf16 (one 128-byte
+// swizzle row) at a time: its 128 rows of A and its 128-row half of B per stage.
+constexpr int kBM = 128;                                   // rows per CTA
+constexpr int kPairM = 2 * kBM;                            // rows per pair tile
+constexpr int kBN = 256;                                   // columns per tile
 constexpr int kBK = 64;
-constexpr int kStages = 4;
+constexpr int kPairBRows = kBN / 2;                        // B rows staged by each CTA
 constexpr int kATileBytes = kBM * kBK * 2;                 // 16 KiB
-constexpr int kBTileBytes = kBN * kBK * 2;                 // 32 KiB
-constexpr int kStageBytes = kATileBytes + kBTileBytes;     // 48 KiB
+constexpr int kPairStageBytes = kATileBytes + kPairBRows * kBK * 2;  // 32 KiB
+constexpr int kPairStages = 6;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;              // TMA warp, MMA warp, epilogue
 constexpr int kTmemCols = 2 * kBN;                         // double-buffered accumulator
 constexpr int kBarrierBytes = 256;
-constexpr size_t kGemmSmemBytes = 1024 + size_t(kStages) * kStageBytes + kBarrierBytes;
+constexpr size_t kPairSmemBytes = 1024 + size_t(kPairStages) * kPairStageBytes + kBarrierBytes;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Persistent tile schedule.  Work is split into units; a unit is one M-tile and a run
-// of `group` consecutive N-tiles (the LSE kernel keeps a running (max, sum) across
-// them).  CTA b takes units b, b + gridDim.x, ...
+// Persistent tile schedule.  Work is split into units; a unit is one 256-row M-tile and
+// a run of `group` consecutive N-tiles (the LSE kernel keeps a running (max, sum)
+// across them).  CTA pair p takes units p, p + pairs, ...
 struct Sched {
   int m_tiles;
   int n_tiles;

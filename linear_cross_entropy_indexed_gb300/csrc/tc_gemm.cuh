@@ -1,19 +1,25 @@
-// Persistent, warp-specialised tcgen05 GEMM engine with pluggable epilogues.
+// Persistent, warp-specialised tcgen05 GEMM engine with pluggable epilogues, run on
+// CTA pairs (a 2-CTA cluster, cta_group::2).
 //
-//   warp 0      TMA producer: stages A (128 x 64) and B (256 x 64) bf16 tiles into a
-//               4-deep shared-memory ring, 128-byte swizzled.
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256, K=16) into
-//               one of two TMEM accumulators (2 x 256 fp32 columns) and commits to
-//               mbarriers that free ring slots / publish finished accumulators.
-//   warps 2..5  epilogue: each warp owns the 32 TMEM lanes (rows) of its lane
+// Each pair computes 256 x 256 output tiles: CTA r of the pair owns output rows
+// [128 r, 128 r + 128) of the tile (its TMEM lanes) and stages, per K step of 64, its
+// own 128 rows of A and its own 128 rows (half) of B, so a stage is 32 KiB and the
+// ring is six stages deep.
+//   warp 0      TMA producer (both CTAs): 128-byte-swizzled boxes into the ring; the
+//               bytes of both CTAs complete on CTA 0's "full" barrier.
+//   warp 1      MMA issuer (one thread of CTA 0): tcgen05.mma.cta_group::2 (M = 256,
+//               N = 256, K = 16) into one of two TMEM accumulators (2 x 256 fp32
+//               columns, allocated pair-wide), committing to both CTAs' barriers.
+//   warps 2..5  epilogue (both CTAs): each warp owns the 32 TMEM lanes of its lane
 //               quadrant, pulls 32 columns at a time with tcgen05.ld and runs the
 //               epilogue (online LSE, dZ, dW store, dH accumulate) while the MMA warp
-//               already fills the other accumulator.
+//               fills the other accumulator; one lane per warp then arrives on CTA 0's
+//               "accumulator empty" barrier.
 //
 // Operands are K-major ([rows, K] with K contiguous) or MN-major ([K, rows] with rows
 // contiguous); both use the 128-byte swizzle that the TMA writes:
-//   K-major : one box {64 K, R rows};    8-row groups 1024 B apart (SBO), K step = +32 B
-//   MN-major: R/64 boxes {64 rows, 64 K}; 64-row atoms 8 KiB apart (LBO), 8-K groups
+//   K-major : one box {64 K, 128 rows};  8-row groups 1024 B apart (SBO), K step = +32 B
+//   MN-major: two boxes {64 rows, 64 K}; 64-row atoms 8 KiB apart (LBO), 8-K groups
 //             1024 B apart (SBO), K step of 16 = +2 KiB
 #pragma once
 
@@ -32,210 +38,12 @@ __device__ __forceinline__ void decode_unit(const Sched& s, int u, int& mt, int&
   }
 }
 
-template <bool MN, int ROWS>
-__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* tm, uint32_t bar,
-                                             int row0, int k0) {
-  if constexpr (!MN) {
-    tma_load_2d(dst, tm, bar, k0, row0);
-  } else {
-#pragma unroll
-    for (int j = 0; j < ROWS / 64; ++j) tma_load_2d(dst + j * 8192, tm, bar, row0 + j * 64, k0);
-  }
-}
-
 template <bool MN>
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int k) {
   if constexpr (!MN) {
     return smem_desc_sw128(base + k * 32, 16, 1024);
   } else {
     return smem_desc_sw128(base + k * 2048, 8192, 1024);
-  }
-}
-
-template <class Epi, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const Sched sched, const typename Epi::Params ep, unsigned long long* err) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  // bars: full[kStages], empty[kStages], tfull[2], tempty[2], drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t tiles_u32 = smem_u32(smem);
-  const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = full0 + 8 * kStages;
-  const uint32_t tfull0 = empty0 + 8 * kStages;
-  const uint32_t tempty0 = tfull0 + 16;
-  const uint32_t drain = tempty0 + 16;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, kEpiWarps * 32);
-    }
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- producer
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t armed = 0;  // bit s: stage s armed at least once; parity of last arm below
-      uint32_t armed_parity = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        int mt, g;
-        decode_unit(sched, u, mt, g);
-        const int nt0 = g * sched.group;
-        const int nt1 = min(nt0 + sched.group, sched.n_tiles);
-        for (int nt = nt0; ok && nt < nt1; ++nt) {
-          for (int kb = 0; kb < sched.k_blocks; ++kb) {
-            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, err)) {
-              ok = false;
-              break;
-            }
-            const uint32_t fb = full0 + 8 * stage;
-            mbar_arrive_expect_tx(fb, kStageBytes);
-            const uint32_t a = tiles_u32 + stage * kStageBytes;
-            load_operand<A_MN, kBM>(a, &tmA, fb, mt * kBM, kb * kBK);
-            load_operand<B_MN, kBN>(a + kATileBytes, &tmB, fb, nt * kBN + sched.b_n_off,
-                                    kb * kBK + sched.b_k_off);
-            armed |= 1u << stage;
-            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1;
-            }
-          }
-        }
-      }
-      if (!ok) {
-        // Let loads already in flight land before the CTA's shared memory goes away.
-        volatile int never = 0;
-        for (int s = 0; s < kStages; ++s)
-          if (armed & (1u << s)) mbar_wait(full0 + 8 * s, (armed_parity >> s) & 1u, &never, err);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, A_MN, B_MN);
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      bool issued = false;
-      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        int mt, g;
-        decode_unit(sched, u, mt, g);
-        const int nt0 = g * sched.group;
-        const int nt1 = min(nt0 + sched.group, sched.n_tiles);
-        for (int nt = nt0; ok && nt < nt1; ++nt) {
-          if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d = tmem_base + acc * kBN;
-          for (int kb = 0; kb < sched.k_blocks; ++kb) {
-            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, err)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t a = tiles_u32 + stage * kStageBytes;
-            const uint32_t b = a + kATileBytes;
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              mma_bf16(d, operand_desc<A_MN>(a, k), operand_desc<B_MN>(b, k), idesc,
-                       (kb | k) != 0 ? 1u : 0u);
-            issued = true;
-            mma_commit(empty0 + 8 * stage);
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1;
-            }
-          }
-          if (!ok) break;
-          mma_commit(tfull0 + 8 * acc);
-          if (++acc == 2) {
-            acc = 0;
-            acc_phase ^= 1;
-          }
-        }
-      }
-      if (!ok && issued) {
-        // Wait (bounded) for every MMA this thread issued before TMEM is released.
-        volatile int never = 0;
-        mma_commit(drain);
-        mbar_wait(drain, 0, &never, err);
-      }
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const int row_in_tile = q * 32 + lane;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-      int mt, g;
-      decode_unit(sched, u, mt, g);
-      const int nt0 = g * sched.group;
-      const int nt1 = min(nt0 + sched.group, sched.n_tiles);
-      const int64_t row = static_cast<int64_t>(mt) * kBM + row_in_tile;
-      typename Epi::State st;
-      Epi::unit_begin(ep, st);
-      for (int nt = nt0; nt < nt1; ++nt) {
-        if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
-        Epi::tile(ep, st, taddr, row, nt);
-        tc_fence_before();
-        mbar_arrive(tempty0 + 8 * acc);
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1;
-        }
-      }
-      if (!ok) break;
-      Epi::unit_end(ep, st, row, g);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -434,18 +242,232 @@ struct EpiDh {
   }
 };
 
+// ====================================================================== engine
+static_assert(kPairSmemBytes <= 232448, "pair pipeline exceeds shared memory");
+
+template <bool MN>
+__device__ __forceinline__ void load_half_pair(uint32_t dst, const CUtensorMap* tm, uint32_t bar_cluster, int row0,
+                                               int k0) {
+  if constexpr (!MN) {
+    tma_load_2d_pair(dst, tm, bar_cluster, k0, row0);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) tma_load_2d_pair(dst + j * 8192, tm, bar_cluster, row0 + j * 64, k0);
+  }
+}
+
+template <class Epi, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const Sched sched, const typename Epi::Params ep, unsigned long long* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const uint32_t tiles_u32 = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kPairStages;
+  const uint32_t tfull0 = empty0 + 8 * kPairStages;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 2 * kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers initialised before any remote arrive / complete_tx
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t full0_lead = mapa_shared(full0, 0);
+  const uint32_t tempty0_lead = mapa_shared(tempty0, 0);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      bool ok = true;
+      for (int u = pair; ok && u < sched.units; u += npairs) {
+        int mt, g;
+        decode_unit(sched, u, mt, g);
+        const int nt0 = g * sched.group;
+        const int nt1 = min(nt0 + sched.group, sched.n_tiles);
+        for (int nt = nt0; ok && nt < nt1; ++nt) {
+          for (int kb = 0; kb < sched.k_blocks; ++kb) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * kPairStageBytes);
+            const uint32_t a = tiles_u32 + stage * kPairStageBytes;
+            const uint32_t fb = full0_lead + 8 * stage;
+            load_half_pair<A_MN>(a, &tmA, fb, mt * kPairM + int(rank) * kBM, kb * kBK);
+            load_half_pair<B_MN>(a + kATileBytes, &tmB, fb, nt * kBN + int(rank) * kPairBRows + sched.b_n_off,
+                                 kb * kBK + sched.b_k_off);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == kPairStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+      }
+      if (!ok && leader) {
+        volatile int never = 0;
+        for (int s = 0; s < kPairStages; ++s)
+          if (armed & (1u << s)) mbar_wait(full0 + 8 * s, (armed_parity >> s) & 1u, &never, err);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------------- MMA issuer (CTA 0)
+      constexpr uint32_t idesc = idesc_bf16_f32(kPairM, kBN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true, issued = false;
+      for (int u = pair; ok && u < sched.units; u += npairs) {
+        int mt, g;
+        decode_unit(sched, u, mt, g);
+        const int nt0 = g * sched.group;
+        const int nt1 = min(nt0 + sched.group, sched.n_tiles);
+        for (int nt = nt0; ok && nt < nt1; ++nt) {
+          if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + acc * kBN;
+          for (int kb = 0; kb < sched.k_blocks; ++kb) {
+            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a = tiles_u32 + stage * kPairStageBytes;
+            const uint32_t b = a + kATileBytes;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_bf16_pair(d, operand_desc<A_MN>(a, k), operand_desc<B_MN>(b, k), idesc, (kb | k) != 0 ? 1u : 0u);
+            issued = true;
+            mma_commit_pair(empty0 + 8 * stage, 0x3);
+            if (++stage == kPairStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          mma_commit_pair(tfull0 + 8 * acc, 0x3);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1;
+          }
+        }
+      }
+      if (!ok && issued) {
+        volatile int never = 0;
+        mma_commit_pair(drain, 0x1);
+        mbar_wait(drain, 0, &never, err);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int row_in_tile = int(rank) * kBM + q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int u = pair; ok && u < sched.units; u += npairs) {
+      int mt, g;
+      decode_unit(sched, u, mt, g);
+      const int nt0 = g * sched.group;
+      const int nt1 = min(nt0 + sched.group, sched.n_tiles);
+      const int64_t row = static_cast<int64_t>(mt) * (2 * kBM) + row_in_tile;
+      typename Epi::State st;
+      Epi::unit_begin(ep, st);
+      for (int nt = nt0; nt < nt1; ++nt) {
+        if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
+        Epi::tile(ep, st, taddr, row, nt);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty0_lead + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      Epi::unit_end(ep, st, row, g);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still touch its barriers or TMEM
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 template <class Epi, bool A_MN, bool B_MN>
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Sched& s,
-                        const typename Epi::Params& p, unsigned long long* err, int grid,
-                        cudaStream_t st) {
-  tc_gemm_kernel<Epi, A_MN, B_MN><<<grid, kThreads, kGemmSmemBytes, st>>>(tmA, tmB, s, p, err);
-  return cudaGetLastError();
+                             const typename Epi::Params& p, unsigned long long* err, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<Epi, A_MN, B_MN>, tmA, tmB, s, p, err);
 }
 
 template <class Epi, bool A_MN, bool B_MN>
 cudaError_t set_smem_attr() {
   return cudaFuncSetAttribute(tc_gemm_kernel<Epi, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kGemmSmemBytes));
+                              static_cast<int>(kPairSmemBytes));
 }
 
 }  // namespace flce
