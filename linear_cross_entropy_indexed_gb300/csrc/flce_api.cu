@@ -15,7 +15,9 @@ namespace flce {
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kLseGroup = 4;                         // vocabulary tiles per forward unit
+constexpr int kLseGroupMin = 4;  // vocabulary tiles per forward unit: range searched
+constexpr int kLseGroupMax = 8;
+constexpr int kPlanPairs = 76;   // SM pairs of a GB300 (152 SMs), for the planner
 constexpr size_t kDefaultChunkBudget = size_t(1) << 30;  // bf16 dZ chunk bytes
 constexpr int kMaxDevices = 64;
 
@@ -128,7 +130,7 @@ int pair_grid(int units, int sms) { return 2 * std::max(1, std::min(units, sms /
 
 // ------------------------------------------------------------------ planning
 struct FwdPlan {
-  int m_tiles = 0, v_tiles = 0, n_groups = 0, k_blocks = 0;
+  int m_tiles = 0, v_tiles = 0, group = 0, n_groups = 0, k_blocks = 0;
   int dot_blocks = 0, merge_blocks = 0;
   size_t off_pm = 0, off_ps = 0, off_t = 0, off_sums = 0, off_counts = 0, total = 0;
 };
@@ -145,17 +147,49 @@ flce_status check_sizes(int64_t N, int64_t Hd, int64_t V) {
   return FLCE_OK;
 }
 
-flce_status plan_forward(int64_t N, int64_t Hd, int64_t V, FwdPlan* p) {
+// Vocabulary tiles per forward unit (4..8): the count whose round-robin assignment of
+// units to the SM pairs has the smallest makespan in tiles (ties: the larger count,
+// which means fewer partials).  Units of one group index share their W tiles.
+int64_t count_congruent(int64_t lo, int64_t hi, int64_t r, int64_t mod) {  // #{u in [lo, hi): u % mod == r}
+  if (hi <= lo) return 0;
+  auto upto = [&](int64_t x) { return x <= r ? int64_t(0) : (x - 1 - r) / mod + 1; };  // #{u in [0, x)}
+  return upto(hi) - upto(lo);
+}
+
+int pick_lse_group(int m_tiles, int v_tiles, int pairs) {
+  int best_g = kLseGroupMin;
+  int64_t best_t = -1;
+  for (int G = kLseGroupMin; G <= kLseGroupMax; ++G) {
+    const int64_t ng = cdiv(v_tiles, G);
+    const int64_t units = int64_t(m_tiles) * ng;
+    const int64_t last = v_tiles - (ng - 1) * G;  // tiles in each unit of the last group
+    int64_t t = 0;
+    for (int p = 0; p < pairs; ++p) {
+      const int64_t all = count_congruent(0, units, p, pairs);
+      const int64_t tail = count_congruent((ng - 1) * m_tiles, units, p, pairs);
+      t = std::max(t, G * all - (G - last) * tail);
+    }
+    if (best_t < 0 || t <= best_t) {
+      best_t = t;
+      best_g = G;
+    }
+  }
+  return best_g;
+}
+
+flce_status plan_forward(int64_t N, int64_t Hd, int64_t V, int pairs, FwdPlan* p) {
   flce_status s = check_sizes(N, Hd, V);
   if (s != FLCE_OK) return s;
   p->m_tiles = cdiv(N, kPairM);  // CTA pairs: 256 token rows per tile
   p->v_tiles = cdiv(V, kBN);
-  p->n_groups = cdiv(p->v_tiles, kLseGroup);
+  p->group = pick_lse_group(p->m_tiles, p->v_tiles, pairs);
+  p->n_groups = cdiv(p->v_tiles, p->group);
   p->k_blocks = cdiv(Hd, kBK);
   p->dot_blocks = static_cast<int>(std::min<int64_t>(std::max<int64_t>(cdiv(N, kDotWarps), 1), kDotMaxBlocks));
   p->merge_blocks = std::max(cdiv(N, kMergeThreads), 1);
   size_t cur = 0, part;
-  if (!mul_ok(size_t(p->n_groups), size_t(N), &part) || !mul_ok(part, 4, &part)) return FLCE_ERR_OVERFLOW;
+  if (!mul_ok(size_t(p->n_groups) * kEpiSplit, size_t(N), &part) || !mul_ok(part, 4, &part))
+    return FLCE_ERR_OVERFLOW;
   if (!reserve(&cur, part, &p->off_pm) || !reserve(&cur, part, &p->off_ps) ||
       !reserve(&cur, size_t(N) * 4, &p->off_t) || !reserve(&cur, size_t(p->merge_blocks) * 8, &p->off_sums) ||
       !reserve(&cur, size_t(p->dot_blocks) * 8, &p->off_counts))
@@ -202,7 +236,7 @@ extern "C" {
 
 size_t flce_forward_workspace_size(int64_t N, int64_t Hd, int64_t V) {
   FwdPlan p;
-  return plan_forward(N, Hd, V, &p) == FLCE_OK ? p.total : 0;
+  return plan_forward(N, Hd, V, kPlanPairs, &p) == FLCE_OK ? p.total : 0;
 }
 
 size_t flce_backward_workspace_size(int64_t N, int64_t Hd, int64_t V, size_t chunk_budget_bytes) {
@@ -216,7 +250,7 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* labels, in
                          void* stream) {
   if (reduction < 0 || reduction > 2 || softcap != softcap) return FLCE_ERR_ARG;
   FwdPlan pl;
-  flce_status s = plan_forward(N, Hd, V, &pl);
+  flce_status s = plan_forward(N, Hd, V, kPlanPairs, &pl);
   if (s != FLCE_OK) return s;
   if (!W || !loss || !counts) return FLCE_ERR_ARG;
   if (N > 0 && (!H || !labels || !lse || !workspace)) return FLCE_ERR_ARG;
@@ -261,7 +295,7 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* labels, in
   sc.m_tiles = pl.m_tiles;
   sc.n_tiles = pl.v_tiles;
   sc.k_blocks = pl.k_blocks;
-  sc.group = kLseGroup;
+  sc.group = pl.group;
   sc.n_groups = pl.n_groups;
   sc.units = pl.m_tiles * pl.n_groups;
   sc.order = 0;
@@ -273,7 +307,7 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* labels, in
   // (3) fixed-order merge, per-row loss, block sums
   float* loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : nullptr;
   e = launch(FLCE_KERNEL_LSE_MERGE, st, [&] {
-    k_lse_merge<<<pl.merge_blocks, kMergeThreads, 0, st>>>(part_m, part_s, pl.n_groups, N, t_ws, labels,
+    k_lse_merge<<<pl.merge_blocks, kMergeThreads, 0, st>>>(part_m, part_s, pl.n_groups * kEpiSplit, N, t_ws, labels,
                                                            ignore_index, V, lse, loss_rows, sums);
     return cudaGetLastError();
   });

@@ -19,7 +19,10 @@ constexpr int kPairBRows = kBN / 2;                        // B rows staged by e
 constexpr int kATileBytes = kBM * kBK * 2;                 // 16 KiB
 constexpr int kPairStageBytes = kATileBytes + kPairBRows * kBK * 2;  // 32 KiB
 constexpr int kPairStages = 6;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 4;                               // a multiple of 4
+constexpr int kEpiSplit = kEpiWarps / 4;                   // warps per TMEM lane quadrant
+constexpr int kSlices = kBN / 32;                          // 32-column slices per tile
+constexpr int kSlicesPerWarp = kSlices / kEpiSplit;        // slices each epilogue warp drains
 constexpr int kThreads = 64 + 32 * kEpiWarps;              // TMA warp, MMA warp, epilogue
 constexpr int kTmemCols = 2 * kBN;                         // double-buffered accumulator
 constexpr int kBarrierBytes = 256;
@@ -54,8 +57,8 @@ struct RowInfo {
 struct EpiLseParams {
   int64_t N, V;
   float softcap;        // <= 0: off
-  float* part_m;        // [n_groups][N], running max in log2 units
-  float* part_s;        // [n_groups][N], sum of 2^(z*log2e - max)
+  float* part_m;        // [n_groups * kEpiSplit][N], running max in log2 units
+  float* part_s;        // [n_groups * kEpiSplit][N], sum of 2^(z*log2e - max)
 };
 
 struct EpiDzParams {

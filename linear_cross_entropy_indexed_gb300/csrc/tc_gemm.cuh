@@ -48,12 +48,26 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int k) {
 }
 
 // ====================================================================== epilogues
-// Tanh softcap from exp2: tanh(u) = 1 - 2 / (e^{2u} + 1), with e^{2u} = 2^{2u log2 e}.
-// Absolute error of the result is a few fp32 ulps of 1 (no cancellation blow-up for
-// small u, saturates to +-1 for large |u|).
-__device__ __forceinline__ float tanh_via_exp2(float u) {
-  const float e = ex2_approx(u * (2.0f * kLog2e));
-  return 1.0f - 2.0f * rcp_approx(e + 1.0f);
+// Every epilogue thread owns one TMEM lane (output row) and drains slices
+// [h * kSlicesPerWarp, (h + 1) * kSlicesPerWarp) of 32 fp32 columns, h = its warp's
+// column half.  Per-element work is kept to a few FMAs around the MUFU operations.
+
+// tanh(u) = 1 - 2 / (e^{2u} + 1); the caller passes a = 2u log2(e), so e^{2u} = 2^a.
+// Absolute error a few fp32 ulps of 1 (no cancellation blow-up for small u); saturates
+// to +-1 for large |u|.
+__device__ __forceinline__ float tanh_from_exp2_arg(float a) {
+  return fmaf(-2.0f, rcp_approx(ex2_approx(a) + 1.0f), 1.0f);
+}
+
+template <class F>
+__device__ __forceinline__ void for_each_slice(uint32_t taddr, int h, F&& f) {
+#pragma unroll 1
+  for (int c = h * kSlicesPerWarp; c < (h + 1) * kSlicesPerWarp; ++c) {
+    float x[32];
+    __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
+    tmem_ld32(taddr + c * 32, x);
+    f(c, x);
+  }
 }
 
 // Forward: running (max, sum) of 2^(z log2 e) over the unit's vocabulary tiles.
@@ -67,38 +81,48 @@ struct EpiLse {
     st.m = -INFINITY;
     st.s = 0.0f;
   }
-  __device__ static void tile(const Params& p, State& st, uint32_t taddr, int64_t, int nt) {
-    const int64_t v_base = static_cast<int64_t>(nt) * kBN;
-    const bool tail = v_base + kBN > p.V;
-    const bool cap = p.softcap > 0.0f;
-    const float inv_c = cap ? 1.0f / p.softcap : 0.0f;
-    const float c_log2e = p.softcap * kLog2e;
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      float x[32];
-      __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
-      tmem_ld32(taddr + c * 32, x);
-      float cmax = -INFINITY;
+  // z is monotone in its key k (k = x without softcap, k = tanh(x/c) with it), so the
+  // slice max is taken on k and z*log2e = k * zs.
+  template <bool CAP>
+  __device__ static void slices(const Params& p, State& st, uint32_t taddr, int nt, int h) {
+    const int64_t v_tile = static_cast<int64_t>(nt) * kBN;
+    const float k_tanh = CAP ? 2.0f * kLog2e / p.softcap : 0.0f;
+    const float zs = CAP ? p.softcap * kLog2e : kLog2e;
+    for_each_slice(taddr, h, [&](int c, float(&x)[32]) {
+      const int64_t v0 = v_tile + c * 32;
+      if (v0 >= p.V) return;  // the whole slice is past V
+      if (CAP) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float z = cap ? c_log2e * tanh_via_exp2(x[j] * inv_c) : x[j] * kLog2e;
-        if (tail && v_base + c * 32 + j >= p.V) z = -INFINITY;
-        x[j] = z;
-        cmax = fmaxf(cmax, z);
+        for (int j = 0; j < 32; ++j) x[j] = tanh_from_exp2_arg(x[j] * k_tanh);
       }
-      if (cmax == -INFINITY) continue;  // the whole 32-column slice is past V
-      const float mn = fmaxf(st.m, cmax);
+      if (v0 + 32 > p.V) {
+        const int n = static_cast<int>(p.V - v0);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j >= n) x[j] = -INFINITY;
+      }
+      float kmax = x[0];
+#pragma unroll
+      for (int j = 1; j < 32; ++j) kmax = fmaxf(kmax, x[j]);
+      const float mn = fmaxf(st.m, kmax * zs);
       float acc = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc += ex2_approx(x[j] - mn);
+      for (int j = 0; j < 32; ++j) acc += ex2_approx(fmaf(x[j], zs, -mn));
       st.s = st.s * ex2_approx(st.m - mn) + acc;  // 2^-inf = 0 for the first slice
       st.m = mn;
-    }
+    });
   }
-  __device__ static void unit_end(const Params& p, State& st, int64_t row, int g) {
+  __device__ static void tile(const Params& p, State& st, uint32_t taddr, int64_t, int nt, int h) {
+    if (p.softcap > 0.0f)
+      slices<true>(p, st, taddr, nt, h);
+    else
+      slices<false>(p, st, taddr, nt, h);
+  }
+  __device__ static void unit_end(const Params& p, State& st, int64_t row, int g, int h) {
     if (row < p.N) {
-      p.part_m[static_cast<int64_t>(g) * p.N + row] = st.m;
-      p.part_s[static_cast<int64_t>(g) * p.N + row] = st.s;
+      const int64_t k = static_cast<int64_t>(g) * kEpiSplit + h;
+      p.part_m[k * p.N + row] = st.m;
+      p.part_s[k * p.N + row] = st.s;
     }
   }
 };
@@ -113,43 +137,38 @@ struct EpiDz {
   using Params = EpiDzParams;
   struct State {};
   __device__ static void unit_begin(const Params&, State&) {}
-  __device__ static void unit_end(const Params&, State&, int64_t, int) {}
-  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt) {
+  __device__ static void unit_end(const Params&, State&, int64_t, int, int) {}
+  template <bool CAP>
+  __device__ static void slices(const Params& p, uint32_t taddr, int64_t row, int nt, int h) {
     RowInfo ri{0.0f, 0.0f, -1, 0};
     const bool row_ok = row < p.N;
     if (row_ok) ri = p.rows[row];
-    const bool cap = p.softcap > 0.0f;
-    const float inv_c = cap ? 1.0f / p.softcap : 0.0f;
-    const float c_log2e = p.softcap * kLog2e;
+    const float k_tanh = CAP ? 2.0f * kLog2e / p.softcap : 0.0f;
+    const float zs = CAP ? p.softcap * kLog2e : kLog2e;
+    const float neg_scale = -ri.scale;
     const int64_t vl_tile = static_cast<int64_t>(nt) * kBN;
     const int64_t y_local = ri.label >= 0 ? static_cast<int64_t>(ri.label) - p.v0 : -1;
     __nv_bfloat16* out_row = p.dz + (row_ok ? row : 0) * p.ldz;
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      float x[32];
-      __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
-      tmem_ld32(taddr + c * 32, x);
+    for_each_slice(taddr, h, [&](int c, float(&x)[32]) {
       const int64_t vl = vl_tile + c * 32;
-      if (!row_ok || vl >= p.wc) continue;
+      if (!row_ok || vl >= p.wc) return;
+      const int yrel = (y_local >= vl && y_local < vl + 32) ? static_cast<int>(y_local - vl) : -1;
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         float d[2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float xv = x[j + h];
-          float z2, dcap;
-          if (cap) {
-            const float t = tanh_via_exp2(xv * inv_c);
-            z2 = c_log2e * t;
-            dcap = 1.0f - t * t;
+        for (int e = 0; e < 2; ++e) {
+          float dv;
+          if (CAP) {
+            const float t = tanh_from_exp2_arg(x[j + e] * k_tanh);
+            const float pr = ex2_approx(fmaf(t, zs, -ri.lse2));
+            dv = fmaf(pr, ri.scale, (j + e == yrel) ? neg_scale : 0.0f) * fmaf(-t, t, 1.0f);
           } else {
-            z2 = xv * kLog2e;
-            dcap = 1.0f;
+            const float pr = ex2_approx(fmaf(x[j + e], zs, -ri.lse2));
+            dv = fmaf(pr, ri.scale, (j + e == yrel) ? neg_scale : 0.0f);
           }
-          float g = ex2_approx(z2 - ri.lse2);
-          if (vl + j + h == y_local) g -= 1.0f;
-          d[h] = g * ri.scale * dcap;
+          d[e] = dv;
         }
         pk[j / 2] = pack_bf16x2(d[0], d[1]);
       }
@@ -164,7 +183,13 @@ struct EpiDz {
           reinterpret_cast<uint16_t*>(out_row)[vl + j] = hbits;
         }
       }
-    }
+    });
+  }
+  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h) {
+    if (p.softcap > 0.0f)
+      slices<true>(p, taddr, row, nt, h);
+    else
+      slices<false>(p, taddr, row, nt, h);
   }
 };
 
@@ -173,17 +198,13 @@ struct EpiDw {
   using Params = EpiDwParams;
   struct State {};
   __device__ static void unit_begin(const Params&, State&) {}
-  __device__ static void unit_end(const Params&, State&, int64_t, int) {}
-  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt) {
+  __device__ static void unit_end(const Params&, State&, int64_t, int, int) {}
+  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h) {
     const bool row_ok = row < p.rows_valid;
     __nv_bfloat16* out_row = p.out + (p.row0 + (row_ok ? row : 0)) * p.cols;
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      float x[32];
-      __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
-      tmem_ld32(taddr + c * 32, x);
+    for_each_slice(taddr, h, [&](int c, float(&x)[32]) {
       const int64_t col = static_cast<int64_t>(nt) * kBN + c * 32;
-      if (!row_ok || col >= p.cols) continue;
+      if (!row_ok || col >= p.cols) return;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         if (col + 8 * k + 8 <= p.cols) {
@@ -192,7 +213,7 @@ struct EpiDw {
           *reinterpret_cast<uint4*>(out_row + col + 8 * k) = v;
         }
       }
-    }
+    });
   }
 };
 
@@ -201,17 +222,13 @@ struct EpiDh {
   using Params = EpiDhParams;
   struct State {};
   __device__ static void unit_begin(const Params&, State&) {}
-  __device__ static void unit_end(const Params&, State&, int64_t, int) {}
-  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt) {
+  __device__ static void unit_end(const Params&, State&, int64_t, int, int) {}
+  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h) {
     const bool row_ok = row < p.N;
     const int64_t base = (row_ok ? row : 0) * p.Hd;
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      float x[32];
-      __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
-      tmem_ld32(taddr + c * 32, x);
+    for_each_slice(taddr, h, [&](int c, float(&x)[32]) {
       const int64_t col = static_cast<int64_t>(nt) * kBN + c * 32;
-      if (!row_ok || col >= p.Hd) continue;
+      if (!row_ok || col >= p.Hd) return;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int64_t cc = col + 8 * k;
@@ -238,7 +255,7 @@ struct EpiDh {
           *reinterpret_cast<float4*>(a + 4) = make_float4(x[8 * k + 4], x[8 * k + 5], x[8 * k + 6], x[8 * k + 7]);
         }
       }
-    }
+    });
   }
 };
 
@@ -403,7 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ epilogue (both CTAs)
-    const int q = warp & 3;
+    const int q = warp & 3;               // TMEM lane quadrant this warp may access
+    const int h = (warp - 2) / 4;         // column half of the tile this warp drains
     const int row_in_tile = int(rank) * kBM + q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -423,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
-        Epi::tile(ep, st, taddr, row, nt);
+        Epi::tile(ep, st, taddr, row, nt, h);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(tempty0_lead + 8 * acc);
@@ -433,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      Epi::unit_end(ep, st, row, g);
+      Epi::unit_end(ep, st, row, g, h);
     }
   }
 

@@ -54,11 +54,12 @@ def test_workspace_sizes(lib):
     assert f(256, 64, 2000) > 0
     assert f(0, 64, 2000) > 0 or f(0, 64, 2000) == 0
     assert f(-1, 64, 2000) == 0 and f(8, 63, 100) == 0 and f(8, 64, 0) == 0
-    # forward scratch is O(N * V / 1024) (one (max, sum) pair per row per 1024-column group)
+    # forward scratch is O(N * V / 1024): one (max, sum) pair per row per group of 4 to 8
+    # vocabulary tiles of 256 columns
     n, hd, v = 8192, 4096, 128256
-    groups = -(-(-(-v // 256)) // 4)
-    assert f(n, hd, v) >= 2 * groups * n * 4
-    assert f(n, hd, v) < 2 * groups * n * 4 + (1 << 20)
+    tiles = -(-v // 256)
+    assert f(n, hd, v) >= 2 * (-(-tiles // 8)) * n * 4
+    assert f(n, hd, v) < 2 * (-(-tiles // 4)) * n * 4 + (1 << 20)
     # backward: one bf16 [N, Vc] chunk plus an fp32 [N, Hd] accumulator when chunked
     budget = 64 << 20
     vc = (budget // (2 * n)) // 256 * 256
