@@ -216,7 +216,8 @@ def run_ours(args, w):
 
     # inputs: each rank its own batch (seed offset by rank), resident in HBM
     wr = S.scaled(w.name, seed=w.seed + 1000 * rank) if rank else w
-    Hb, Wb, yb = S.make_H(wr), S.make_W(wr), S.make_labels(wr)
+    Wb = S.make_W(wr)
+    Hb, yb = S.make_H(wr, W=Wb), S.make_labels(wr)
     to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(dev)
     H, W = to_dev(Hb), to_dev(Wb)
     y = torch.from_numpy(yb).to(dev)
@@ -232,7 +233,7 @@ def run_ours(args, w):
     def step():
         loss, lse, counts, _ = F.flce_forward(H, W, y, w.ignore_index, w.softcap, red, workspace=workspace)
         F.flce_backward(H, W, y, lse, counts, g, w.ignore_index, w.softcap, red, budget, workspace=workspace,
-                        dH=dH, dW=dW)
+                        dH=dH, dW=dW, filter_threshold=args.filter_threshold)
         return loss, counts
 
     for _ in range(args.warmup):
@@ -308,7 +309,8 @@ def run_ours(args, w):
             yd_.copy_(yh, non_blocking=True)
             Hx = Hd_.detach().requires_grad_(True)
             Wx = Wd_.detach().requires_grad_(True)
-            loss = F.linear_cross_entropy(Hx, Wx, yd_, w.ignore_index, w.softcap, red, budget)
+            loss = F.linear_cross_entropy(Hx, Wx, yd_, w.ignore_index, w.softcap, red, budget,
+                                          args.filter_threshold)
             loss.backward()
             return loss.item()
 
@@ -336,7 +338,7 @@ def run_ours(args, w):
     Wx = W.detach().requires_grad_(True)
     torch.cuda.reset_peak_memory_stats(dev)
     base = torch.cuda.memory_allocated(dev)
-    loss = F.linear_cross_entropy(Hx, Wx, y, w.ignore_index, w.softcap, red, budget)
+    loss = F.linear_cross_entropy(Hx, Wx, y, w.ignore_index, w.softcap, red, budget, args.filter_threshold)
     loss.backward()
     torch.cuda.synchronize()
     peak = torch.cuda.max_memory_allocated(dev) - base
@@ -355,7 +357,10 @@ def run_ours(args, w):
             "config": {"workload": workload_desc(w), "global_batch": ws * N, "seq_len": 4096 if N >= 4096 else N,
                        "parallelism": "dp%d" % ws if ws > 1 else "single",
                        "l2": "inputs larger than L2 (W %.0f MiB > 129 MB); no flush" % (W.numel() * 2 / 2**20),
-                       "chunk_budget_bytes": budget or (1 << 30)},
+                       "chunk_budget_bytes": budget or (1 << 30),
+                       "filter_threshold": args.filter_threshold},
+            # flops counted as the exact path's 8*N*Hd*V; a filtered run skips part of it
+            "flops_basis": "8*N*Hd*V" + (" (exact work; filtering skips some)" if args.filter_threshold > 0 else ""),
             "pct_bf16_peak": 100.0 * flops / (ms * 1e-3) / (peaks["bf16"] * 1e12),
             "pct_bf16_peak_sustained": 100.0 * flops / (ms * 1e-3) / (peaks["bf16_sus"] * 1e12),
             "peak_extra_mb": peak_extra_mb,
@@ -384,6 +389,8 @@ def main():
     ap.add_argument("--config", default="llama3")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--chunk-budget", type=int, default=0)
+    ap.add_argument("--filter-threshold", type=float, default=0.0,
+                    help="gradient filtering threshold (0 = exact backward; e.g. 2**-12 = 0.000244140625)")
     ap.add_argument("--cpu-sample", type=int, default=1024)
     ap.add_argument("--ref-sample", type=int, default=64)
     ap.add_argument("--no-e2e", action="store_true")

@@ -57,12 +57,12 @@ extern "C" {
 
 typedef enum flce_status {
   FLCE_OK = 0,
-  FLCE_ERR_ARG = 1,          /* null pointer, negative size, unknown reduction        */
+  FLCE_ERR_ARG = 1,          /* null pointer, negative size, unknown reduction, NaN    */
   FLCE_ERR_ALIGN = 2,        /* a base address is not 16-byte aligned, or Hd % 8 != 0 */
   FLCE_ERR_WORKSPACE = 3,    /* workspace smaller than the size query, or not 256-B aligned */
   FLCE_ERR_OVERFLOW = 4,     /* a size overflows 64-bit byte counts or the 2^31 TMA limits */
   FLCE_ERR_CUDA = 5,         /* a CUDA runtime call failed; see flce_last_cuda_error() */
-  FLCE_ERR_UNSUPPORTED = 6   /* device is not sm_103, or a feature not built (filtering) */
+  FLCE_ERR_UNSUPPORTED = 6   /* device is not sm_103                                    */
 } flce_status;
 
 typedef enum flce_reduction {
@@ -80,7 +80,8 @@ FLCE_API size_t flce_forward_workspace_size(int64_t N, int64_t Hd, int64_t V);
 
 /* Bytes of scratch that flce_backward needs.  The backward walks the vocabulary in
    chunks of Vc columns and keeps one bf16 [N, Vc] dZ chunk plus an fp32 [N, Hd] dH
-   accumulator (the latter only when there is more than one chunk).
+   accumulator (the latter only when there is more than one chunk), plus one byte per
+   64 x 64 block of the chunk for the filtered mode.
    chunk_budget_bytes bounds the dZ chunk (0 = default 1 GiB); the same value must be
    passed to flce_backward. */
 FLCE_API size_t flce_backward_workspace_size(int64_t N, int64_t Hd, int64_t V, size_t chunk_budget_bytes);
@@ -112,7 +113,12 @@ FLCE_API flce_status flce_forward(const void* H, const void* W, const int64_t* l
  *   counts       (device) int64 [3] from flce_forward; counts[0] (n_valid) scales the
  *                mean; error bits are OR-ed into counts[2]
  *   grad_out     (device) fp32 [1] (MEAN/SUM) or [N] (NONE): upstream gradient
- *   filter_threshold  must be 0 (exact backward); tile skipping is not built
+ *   filter_threshold  0: exact backward.  > 0: gradient filtering (Liger-CCE blog, §三
+ *                "CCE": softmax entries below 2^-12 vanish in a bf16 gradient): entries with
+ *                p < threshold other than a valid row's target are dropped from dZ, and
+ *                every 64 x 64 (token x vocabulary) block of dZ left all zero is skipped
+ *                by the dW and dH products.  An approximation; the exact path is the
+ *                default.  Negative or NaN: FLCE_ERR_ARG.
  *   dH           (device) bf16 [N, Hd] (written)
  *   dW           (device) bf16 [V, Hd] (written, every row)
  *   workspace    (device) >= flce_backward_workspace_size(N, Hd, V, chunk_budget_bytes)
@@ -177,6 +183,7 @@ FLCE_API int flce_last_cuda_error(void);
 #define FLCE_KERNEL_DW 6          /* tensor-core dW chunk = dZ^T H                     */
 #define FLCE_KERNEL_DH 7          /* tensor-core dH += dZ W_chunk                      */
 #define FLCE_KERNEL_ZERO 8        /* zero fill (dW when N == 0)                        */
+#define FLCE_KERNEL_BLOCK_MASK 9  /* filtered backward: live K steps per dW / dH tile   */
 FLCE_API uint64_t flce_launch_count(void);
 FLCE_API int flce_set_event_sink(void* const* start_events, void* const* end_events, int* kernel_ids,
                         int capacity);

@@ -34,7 +34,7 @@ __all__ = [
 
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 KERNEL_NAMES = {0: "label_dot", 1: "linear_lse", 2: "lse_merge", 3: "reduce", 4: "bwd_prep",
-                5: "dz", 6: "dw", 7: "dh", 8: "zero"}
+                5: "dz", 6: "dw", 7: "dh", 8: "zero", 9: "block_mask"}
 
 _lock = threading.Lock()
 _lib = None
@@ -148,8 +148,11 @@ def flce_forward(H, W, labels, ignore_index: int = -100, softcap: float = 0.0, r
 
 
 def flce_backward(H, W, labels, lse, counts, grad_out, ignore_index: int = -100, softcap: float = 0.0,
-                  reduction="mean", chunk_budget: int = 0, workspace=None, dH=None, dW=None):
-    """One backward call from the saved LSE and counts.  Returns (dH, dW) in bf16."""
+                  reduction="mean", chunk_budget: int = 0, workspace=None, dH=None, dW=None,
+                  filter_threshold: float = 0.0):
+    """One backward call from the saved LSE and counts.  Returns (dH, dW) in bf16.
+    filter_threshold > 0 turns on gradient filtering (softmax entries below it, other
+    than the target, are dropped and all-zero blocks are skipped): an approximation."""
     _check_inputs(H, W, labels)
     red = _reduction(reduction)
     N, Hd = H.shape
@@ -164,7 +167,8 @@ def flce_backward(H, W, labels, lse, counts, grad_out, ignore_index: int = -100,
         need = backward_workspace_size(N, Hd, V, chunk_budget)
         ws = workspace if workspace is not None else torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         _check(library().flce_backward(_p(H), _p(W), _p(labels), _p(lse), _p(counts), N, Hd, V, int(ignore_index),
-                                       float(softcap), red, _p(g), 0.0, _p(dH), _p(dW), _p(ws), ws.numel(),
+                                       float(softcap), red, _p(g), float(filter_threshold), _p(dH), _p(dW), _p(ws),
+                                       ws.numel(),
                                        int(chunk_budget), _stream(dev)))
     return dH, dW
 
@@ -182,31 +186,33 @@ def check_counts(counts) -> tuple[int, int]:
 
 class _FusedLinearCrossEntropy(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, H, W, labels, ignore_index, softcap, reduction, chunk_budget):
+    def forward(ctx, H, W, labels, ignore_index, softcap, reduction, chunk_budget, filter_threshold):
         loss, lse, counts, _ = flce_forward(H, W, labels, ignore_index, softcap, reduction)
         ctx.save_for_backward(H, W, labels, lse, counts)
-        ctx.cfg = (ignore_index, softcap, reduction, chunk_budget)
+        ctx.cfg = (ignore_index, softcap, reduction, chunk_budget, filter_threshold)
         return loss
 
     @staticmethod
     def backward(ctx, grad):
         H, W, labels, lse, counts = ctx.saved_tensors
-        ignore_index, softcap, reduction, chunk_budget = ctx.cfg
-        dH, dW = flce_backward(H, W, labels, lse, counts, grad, ignore_index, softcap, reduction, chunk_budget)
+        ignore_index, softcap, reduction, chunk_budget, filter_threshold = ctx.cfg
+        dH, dW = flce_backward(H, W, labels, lse, counts, grad, ignore_index, softcap, reduction, chunk_budget,
+                               filter_threshold=filter_threshold)
         return (dH if ctx.needs_input_grad[0] else None, dW if ctx.needs_input_grad[1] else None,
-                None, None, None, None, None)
+                None, None, None, None, None, None)
 
 
 def linear_cross_entropy(hidden, weight, labels, ignore_index: int = -100, softcap: float = 0.0,
-                         reduction: str = "mean", chunk_budget: int = 0):
+                         reduction: str = "mean", chunk_budget: int = 0, filter_threshold: float = 0.0):
     """Cross-entropy of ``hidden @ weight.T`` against ``labels`` without materialising
     the logits.  ``hidden`` [..., Hd] bf16, ``weight`` [V, Hd] bf16, ``labels`` [...]
-    int64.  reduction: "mean" (over rows whose label is valid), "sum" or "none"."""
+    int64.  reduction: "mean" (over rows whose label is valid), "sum" or "none".
+    filter_threshold > 0 (e.g. 2**-12) makes the backward approximate: see flce_backward."""
     Hd = hidden.shape[-1]
     H2 = hidden.reshape(-1, Hd)
     y = labels.reshape(-1)
     out = _FusedLinearCrossEntropy.apply(H2.contiguous(), weight.contiguous(), y.contiguous(), int(ignore_index),
-                                         float(softcap), reduction, int(chunk_budget))
+                                         float(softcap), reduction, int(chunk_budget), float(filter_threshold))
     if reduction == "none":
         out = out.reshape(labels.shape)
     return out

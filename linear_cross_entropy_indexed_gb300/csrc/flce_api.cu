@@ -201,7 +201,9 @@ flce_status plan_forward(int64_t N, int64_t Hd, int64_t V, int pairs, FwdPlan* p
 struct BwdPlan {
   int64_t Vc = 0;
   int n_chunks = 0;
-  size_t off_rows = 0, off_dz = 0, off_dh = 0, total = 0;
+  int nz_rows = 0, nz_ld = 0;  // token blocks x vocabulary blocks of the dZ block flags
+  int dh_mask_ld = 0, dw_mask_ld = 0, mask_tok_tiles = 0, mask_voc_tiles = 0;
+  size_t off_rows = 0, off_dz = 0, off_dh = 0, off_nz = 0, off_dh_mask = 0, off_dw_mask = 0, total = 0;
 };
 
 flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, BwdPlan* p) {
@@ -215,11 +217,19 @@ flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, BwdPl
   if (vc > v_round) vc = v_round;
   p->Vc = vc;
   p->n_chunks = cdiv(V, vc);
+  p->nz_rows = cdiv(N, 64);
+  p->nz_ld = static_cast<int>(vc / 64);
+  p->dh_mask_ld = cdiv(p->nz_ld, 32);
+  p->dw_mask_ld = cdiv(p->nz_rows, 32);
+  p->mask_tok_tiles = cdiv(N, kPairM);
+  p->mask_voc_tiles = static_cast<int>(vc / kPairM);
   size_t cur = 0, dz, dh = 0;
   if (!mul_ok(size_t(N), size_t(vc), &dz) || !mul_ok(dz, 2, &dz)) return FLCE_ERR_OVERFLOW;
   if (p->n_chunks > 1 && (!mul_ok(size_t(N), size_t(Hd), &dh) || !mul_ok(dh, 4, &dh))) return FLCE_ERR_OVERFLOW;
   if (!reserve(&cur, size_t(N) * sizeof(RowInfo), &p->off_rows) || !reserve(&cur, dz, &p->off_dz) ||
-      !reserve(&cur, dh, &p->off_dh))
+      !reserve(&cur, dh, &p->off_dh) || !reserve(&cur, size_t(p->nz_rows) * size_t(p->nz_ld), &p->off_nz) ||
+      !reserve(&cur, size_t(p->mask_tok_tiles) * p->dh_mask_ld * 4, &p->off_dh_mask) ||
+      !reserve(&cur, size_t(p->mask_voc_tiles) * p->dw_mask_ld * 4, &p->off_dw_mask))
     return FLCE_ERR_OVERFLOW;
   p->total = align_up(cur);
   return FLCE_OK;
@@ -326,9 +336,8 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
                           int64_t N, int64_t Hd, int64_t V, int64_t ignore_index, float softcap, int reduction,
                           const float* grad_out, float filter_threshold, void* dH, void* dW, void* workspace,
                           size_t workspace_bytes, size_t chunk_budget_bytes, void* stream) {
-  if (reduction < 0 || reduction > 2 || softcap != softcap || filter_threshold != filter_threshold)
-    return FLCE_ERR_ARG;
-  if (filter_threshold != 0.0f) return FLCE_ERR_UNSUPPORTED;
+  if (reduction < 0 || reduction > 2 || softcap != softcap || !(filter_threshold >= 0.0f)) return FLCE_ERR_ARG;
+  const bool filter = filter_threshold > 0.0f;
   BwdPlan pl;
   flce_status s = plan_backward(N, Hd, V, chunk_budget_bytes, &pl);
   if (s != FLCE_OK) return s;
@@ -352,6 +361,11 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
   RowInfo* rows = reinterpret_cast<RowInfo*>(ws + pl.off_rows);
   __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_dz);
   float* dh32 = pl.n_chunks > 1 ? reinterpret_cast<float*>(ws + pl.off_dh) : nullptr;
+  uint8_t* nz = filter ? ws + pl.off_nz : nullptr;
+  uint32_t* dh_mask = reinterpret_cast<uint32_t*>(ws + pl.off_dh_mask);
+  uint32_t* dw_mask = reinterpret_cast<uint32_t*>(ws + pl.off_dw_mask);
+  // skipping needs a tile's mask to fit the kernels' shared-memory copy
+  const bool skip = filter && pl.dh_mask_ld <= kMaskWords && pl.dw_mask_ld <= kMaskWords;
   unsigned long long* err = reinterpret_cast<unsigned long long*>(counts + 2);
 
   e = launch(FLCE_KERNEL_BWD_PREP, st, [&] {
@@ -384,10 +398,24 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
     s4.units = s4.m_tiles * s4.n_groups;
     s4.order = 0;
     s4.b_n_off = static_cast<int>(v0);
-    EpiDzParams p4{N, V, v0, wc, pl.Vc, softcap, rows, dz};
+    if (filter && (e = cudaMemsetAsync(nz, 0, size_t(pl.nz_rows) * size_t(pl.nz_ld), st)) != cudaSuccess)
+      return cuda_fail(e);
+    EpiDzParams p4{N, V, v0, wc, pl.Vc, softcap, rows, dz, filter_threshold, nz, pl.nz_ld};
     e = launch(FLCE_KERNEL_DZ, st,
                [&] { return launch_dz(tmH_k, tmW_k, s4, p4, err, pair_grid(s4.units, sms), st); });
     if (e != cudaSuccess) return cuda_fail(e);
+
+    if (skip) {  // per-tile K-step masks of the dW and dH products
+      const int kb_dh = cdiv(wc, kBK);
+      const int vt = cdiv(wc, kPairM);
+      const int total = pl.mask_tok_tiles * pl.dh_mask_ld + vt * pl.dw_mask_ld;
+      e = launch(FLCE_KERNEL_BLOCK_MASK, st, [&] {
+        k_block_masks<<<std::min(cdiv(total, 256), 4 * sms), 256, 0, st>>>(
+            nz, pl.nz_rows, pl.nz_ld, kb_dh, pl.mask_tok_tiles, vt, dh_mask, pl.dh_mask_ld, dw_mask, pl.dw_mask_ld);
+        return cudaGetLastError();
+      });
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
 
     // dW rows [v0, v0 + wc) = dZ_chunk^T H
     Sched s5{};
@@ -398,6 +426,10 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
     s5.n_groups = d_tiles;
     s5.units = s5.m_tiles * s5.n_groups;
     s5.order = 1;
+    if (skip) {
+      s5.kmask = dw_mask;
+      s5.kmask_ld = pl.dw_mask_ld;
+    }
     EpiDwParams p5{wc, v0, Hd, static_cast<__nv_bfloat16*>(dW)};
     e = launch(FLCE_KERNEL_DW, st,
                [&] { return launch_dw(tmDz_mn, tmH_mn, s5, p5, err, pair_grid(s5.units, sms), st); });
@@ -413,6 +445,10 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
     s6.units = s6.m_tiles * s6.n_groups;
     s6.order = 1;
     s6.b_k_off = static_cast<int>(v0);
+    if (skip) {
+      s6.kmask = dh_mask;
+      s6.kmask_ld = pl.dh_mask_ld;
+    }
     EpiDhParams p6{N, Hd, dh32, static_cast<__nv_bfloat16*>(dH), c == 0, c == pl.n_chunks - 1};
     e = launch(FLCE_KERNEL_DH, st,
                [&] { return launch_dh(tmDz_k, tmW_mn, s6, p6, err, pair_grid(s6.units, sms), st); });
@@ -424,12 +460,12 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
 const char* flce_strerror(int status) {
   switch (status) {
     case FLCE_OK: return "ok";
-    case FLCE_ERR_ARG: return "invalid argument (null pointer, negative size, unknown reduction or NaN)";
+    case FLCE_ERR_ARG: return "invalid argument (null pointer, negative size, unknown reduction, NaN or negative threshold)";
     case FLCE_ERR_ALIGN: return "misaligned pointer or hidden size not a multiple of 8";
     case FLCE_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
     case FLCE_ERR_OVERFLOW: return "sizes overflow the 64-bit byte counts or the 2^31 index limits";
     case FLCE_ERR_CUDA: return "a CUDA runtime call failed (see flce_last_cuda_error)";
-    case FLCE_ERR_UNSUPPORTED: return "unsupported device (needs sm_103) or feature not built";
+    case FLCE_ERR_UNSUPPORTED: return "unsupported device (needs sm_103)";
     default: return "unknown status";
   }
 }

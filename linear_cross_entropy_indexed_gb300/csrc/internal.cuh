@@ -26,7 +26,9 @@ constexpr int kSlicesPerWarp = kSlices / kEpiSplit;        // slices each epilog
 constexpr int kThreads = 64 + 32 * kEpiWarps;              // TMA warp, MMA warp, epilogue
 constexpr int kTmemCols = 2 * kBN;                         // double-buffered accumulator
 constexpr int kBarrierBytes = 256;
-constexpr size_t kPairSmemBytes = 1024 + size_t(kPairStages) * kPairStageBytes + kBarrierBytes;
+constexpr int kMaskWords = 512;                            // K-step bitmask words (16384 steps)
+constexpr size_t kPairSmemBytes =
+    1024 + size_t(kPairStages) * kPairStageBytes + kBarrierBytes + 2 * kMaskWords * sizeof(uint32_t);
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -44,6 +46,11 @@ struct Sched {
   int order;     // 0: consecutive units walk M first (share the B operand); 1: walk N first
   int b_n_off;   // added to the B operand's N coordinate (rows of W, K-major B)
   int b_k_off;   // added to the B operand's K coordinate (rows of W, MN-major B)
+  // Block skipping over a filtered dZ chunk (null: off): per pair tile (M index), a
+  // bitmask of its K steps whose dZ slab holds a non-zero entry, kmask_ld words per tile.
+  // A K step whose slab is all zero is neither loaded nor multiplied.
+  const uint32_t* kmask;
+  int kmask_ld;
 };
 
 // Per-row data the dZ epilogue needs, packed in one 16-byte load.
@@ -69,6 +76,9 @@ struct EpiDzParams {
   float softcap;
   const RowInfo* rows;
   __nv_bfloat16* dz;
+  float filter;         // drop entries with p < filter off the target (0: exact)
+  uint8_t* nz;          // block flags written when filtering, else null
+  int nz_ld;            // vocabulary blocks per token-block row of nz
 };
 
 struct EpiDwParams {

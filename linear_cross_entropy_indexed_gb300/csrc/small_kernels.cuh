@@ -176,4 +176,44 @@ __global__ void k_bwd_prep(const int64_t* __restrict__ labels, const float* __re
   out[i] = r;
 }
 
+// Bitmasks of the live K steps of the dW and dH products over a filtered dZ chunk.
+// nz is [TB][VB] bytes, one per 64 x 64 (token x vocabulary) block, non-zero when the
+// block holds a non-zero dZ entry.
+//   dH pair tile mt (token blocks 4mt..4mt+3), K steps = vocabulary blocks kb < kb_dh:
+//     dh_mask[mt * dh_ld + kb / 32] bit kb % 32
+//   dW pair tile vt (vocabulary blocks 4vt..4vt+3), K steps = token blocks tb < TB:
+//     dw_mask[vt * dw_ld + tb / 32] bit tb % 32
+__global__ void k_block_masks(const uint8_t* __restrict__ nz, int TB, int VB, int kb_dh, int MT, int VT,
+                              uint32_t* __restrict__ dh_mask, int dh_ld, uint32_t* __restrict__ dw_mask, int dw_ld) {
+  const int total_dh = MT * dh_ld;
+  const int total = total_dh + VT * dw_ld;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    uint32_t bits = 0;
+    if (i < total_dh) {
+      const int mt = i / dh_ld, w = i - (i / dh_ld) * dh_ld;
+      for (int j = 0; j < 32; ++j) {
+        const int kb = w * 32 + j;
+        if (kb >= kb_dh) break;
+        uint32_t any = 0;
+        for (int t = 0; t < 4; ++t) {
+          const int tb = mt * 4 + t;
+          if (tb < TB) any |= nz[static_cast<int64_t>(tb) * VB + kb];
+        }
+        bits |= (any != 0 ? 1u : 0u) << j;
+      }
+      dh_mask[i] = bits;
+    } else {
+      const int k = i - total_dh;
+      const int vt = k / dw_ld, w = k - (k / dw_ld) * dw_ld;
+      for (int j = 0; j < 32; ++j) {
+        const int tb = w * 32 + j;
+        if (tb >= TB) break;
+        const uint32_t v4 = *reinterpret_cast<const uint32_t*>(nz + static_cast<int64_t>(tb) * VB + vt * 4);
+        bits |= (v4 != 0 ? 1u : 0u) << j;
+      }
+      dw_mask[k] = bits;
+    }
+  }
+}
+
 }  // namespace flce

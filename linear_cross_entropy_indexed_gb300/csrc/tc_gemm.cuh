@@ -133,12 +133,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Backward: recompute the logit tile, dZ = (p - onehot) * scale * cap', bf16 store.
+// With filtering, entries with p below the threshold (other than the target) are
+// dropped and each warp marks the 64 x 64 blocks it wrote a non-zero into.
 struct EpiDz {
   using Params = EpiDzParams;
   struct State {};
   __device__ static void unit_begin(const Params&, State&) {}
   __device__ static void unit_end(const Params&, State&, int64_t, int, int) {}
-  template <bool CAP>
+  template <bool CAP, bool FILTER>
   __device__ static void slices(const Params& p, uint32_t taddr, int64_t row, int nt, int h) {
     RowInfo ri{0.0f, 0.0f, -1, 0};
     const bool row_ok = row < p.N;
@@ -151,27 +153,37 @@ struct EpiDz {
     __nv_bfloat16* out_row = p.dz + (row_ok ? row : 0) * p.ldz;
     for_each_slice(taddr, h, [&](int c, float(&x)[32]) {
       const int64_t vl = vl_tile + c * 32;
-      if (!row_ok || vl >= p.wc) return;
+      if (vl >= p.wc) return;  // same for the whole warp
       const int yrel = (y_local >= vl && y_local < vl + 32) ? static_cast<int>(y_local - vl) : -1;
       uint32_t pk[16];
+      bool nonzero = false;
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         float d[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          float dv;
+          float dv, pr;
           if (CAP) {
             const float t = tanh_from_exp2_arg(x[j + e] * k_tanh);
-            const float pr = ex2_approx(fmaf(t, zs, -ri.lse2));
+            pr = ex2_approx(fmaf(t, zs, -ri.lse2));
             dv = fmaf(pr, ri.scale, (j + e == yrel) ? neg_scale : 0.0f) * fmaf(-t, t, 1.0f);
           } else {
-            const float pr = ex2_approx(fmaf(x[j + e], zs, -ri.lse2));
+            pr = ex2_approx(fmaf(x[j + e], zs, -ri.lse2));
             dv = fmaf(pr, ri.scale, (j + e == yrel) ? neg_scale : 0.0f);
+          }
+          if (FILTER) {
+            if (pr < p.filter && j + e != yrel) dv = 0.0f;
+            nonzero |= dv != 0.0f;
           }
           d[e] = dv;
         }
         pk[j / 2] = pack_bf16x2(d[0], d[1]);
       }
+      if (FILTER) {
+        const unsigned any = __ballot_sync(0xffffffffu, nonzero && row_ok);
+        if (any != 0 && (threadIdx.x & 31) == 0) p.nz[(row / 64) * p.nz_ld + vl / 64] = 1;
+      }
+      if (!row_ok) return;
       if (vl + 32 <= p.wc) {
         uint4* dst = reinterpret_cast<uint4*>(out_row + vl);
 #pragma unroll
@@ -186,10 +198,18 @@ struct EpiDz {
     });
   }
   __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h) {
-    if (p.softcap > 0.0f)
-      slices<true>(p, taddr, row, nt, h);
-    else
-      slices<false>(p, taddr, row, nt, h);
+    const bool cap = p.softcap > 0.0f;
+    if (p.nz != nullptr) {
+      if (cap)
+        slices<true, true>(p, taddr, row, nt, h);
+      else
+        slices<false, true>(p, taddr, row, nt, h);
+    } else {
+      if (cap)
+        slices<true, false>(p, taddr, row, nt, h);
+      else
+        slices<false, false>(p, taddr, row, nt, h);
+    }
   }
 };
 
@@ -262,6 +282,23 @@ struct EpiDh {
 // ====================================================================== engine
 static_assert(kPairSmemBytes <= 232448, "pair pipeline exceeds shared memory");
 
+// Block skipping over a filtered dZ chunk: sched.kmask holds, per pair tile (M index),
+// a bitmask of the K steps whose dZ slab has a non-zero entry (built by k_block_masks).
+// At each tile start the issuing thread copies the tile's words to shared memory with
+// independent loads; producer and MMA thread copy the same words, so they take the
+// same decisions.
+__device__ __forceinline__ void load_kmask(const Sched& s, int mt, uint32_t* mask) {
+  const uint32_t* src = s.kmask + static_cast<int64_t>(mt) * s.kmask_ld;
+  const int words = (s.k_blocks + 31) / 32;
+  for (int w = 0; w < words; ++w) mask[w] = __ldg(src + w);
+}
+
+// A K step is run when active, and the last one is run anyway when none was, so that
+// the accumulator of an all-zero tile is initialised (to zero).
+__device__ __forceinline__ bool kblock_run(const Sched& s, const uint32_t* mask, int kb, int done) {
+  return ((mask[kb >> 5] >> (kb & 31)) & 1u) != 0 || (kb == s.k_blocks - 1 && done == 0);
+}
+
 template <bool MN>
 __device__ __forceinline__ void load_half_pair(uint32_t dst, const CUtensorMap* tm, uint32_t bar_cluster, int row0,
                                                int k0) {
@@ -283,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* kmask = reinterpret_cast<uint32_t*>(smem + kPairStages * kPairStageBytes + kBarrierBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -337,11 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nt0 = g * sched.group;
         const int nt1 = min(nt0 + sched.group, sched.n_tiles);
         for (int nt = nt0; ok && nt < nt1; ++nt) {
-          for (int kb = 0; kb < sched.k_blocks; ++kb) {
-            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, err)) {
-              ok = false;
-              break;
-            }
+          // one K step: wait for a free slot, arm the full barrier, load both halves
+          auto load_step = [&](int kb) -> bool {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, err)) return false;
             if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * kPairStageBytes);
             const uint32_t a = tiles_u32 + stage * kPairStageBytes;
             const uint32_t fb = full0_lead + 8 * stage;
@@ -353,6 +389,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (++stage == kPairStages) {
               stage = 0;
               phase ^= 1;
+            }
+            return true;
+          };
+          if (sched.kmask == nullptr) {
+            for (int kb = 0; kb < sched.k_blocks; ++kb)
+              if (!load_step(kb)) {
+                ok = false;
+                break;
+              }
+          } else {  // filtered dZ: only the K steps of the tile's mask
+            uint32_t* mask = kmask;
+            load_kmask(sched, mt, mask);
+            int done = 0;
+            for (int kb = 0; kb < sched.k_blocks; ++kb) {
+              if (!kblock_run(sched, mask, kb, done)) continue;
+              ++done;
+              if (!load_step(kb)) {
+                ok = false;
+                break;
+              }
             }
           }
         }
@@ -385,22 +441,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d = tmem_base + acc * kBN;
-          for (int kb = 0; kb < sched.k_blocks; ++kb) {
-            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, err)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t a = tiles_u32 + stage * kPairStageBytes;
-            const uint32_t b = a + kATileBytes;
+          if (sched.kmask == nullptr) {
+            for (int kb = 0; kb < sched.k_blocks; ++kb) {
+              if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, err)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a = tiles_u32 + stage * kPairStageBytes;
+              const uint32_t b = a + kATileBytes;
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              mma_bf16_pair(d, operand_desc<A_MN>(a, k), operand_desc<B_MN>(b, k), idesc, (kb | k) != 0 ? 1u : 0u);
-            issued = true;
-            mma_commit_pair(empty0 + 8 * stage, 0x3);
-            if (++stage == kPairStages) {
-              stage = 0;
-              phase ^= 1;
+              for (int k = 0; k < kBK / 16; ++k)
+                mma_bf16_pair(d, operand_desc<A_MN>(a, k), operand_desc<B_MN>(b, k), idesc, (kb | k) != 0 ? 1u : 0u);
+              issued = true;
+              mma_commit_pair(empty0 + 8 * stage, 0x3);
+              if (++stage == kPairStages) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+          } else {  // filtered dZ: only the K steps of the tile's mask
+            uint32_t* mask = kmask + kMaskWords;
+            load_kmask(sched, mt, mask);
+            int done = 0;
+            for (int kb = 0; kb < sched.k_blocks; ++kb) {
+              if (!kblock_run(sched, mask, kb, done)) continue;
+              if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, err)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a = tiles_u32 + stage * kPairStageBytes;
+              const uint32_t b = a + kATileBytes;
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k)
+                mma_bf16_pair(d, operand_desc<A_MN>(a, k), operand_desc<B_MN>(b, k), idesc,
+                              (done | k) != 0 ? 1u : 0u);
+              ++done;
+              issued = true;
+              mma_commit_pair(empty0 + 8 * stage, 0x3);
+              if (++stage == kPairStages) {
+                stage = 0;
+                phase ^= 1;
+              }
             }
           }
           if (!ok) break;

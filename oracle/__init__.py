@@ -26,6 +26,9 @@ What it computes is the plain definition, row by row, in double precision:
 * gradient      dL/dx = (softmax(z) - onehot(y)) * scale_i * cap'(x), with softmax
                 recomputed as exp(z - LSE) from the saved LSE; dH = dZ W, dW = dZ^T H
                 (ai-infra-kb M011, §06; Liger-CCE blog "一、这堵墙" observation 1)
+* filtering     optionally, softmax entries below a threshold (other than a valid row's
+                target) are dropped before forming dZ: CCE's gradient filtering
+                (Liger-CCE blog, §三), an approximation of the exact gradient
 
 ``forward_split`` is a blockwise restatement (row chunks x vocab chunks merged with
 the running (m, s) rule of ai-infra-kb M011 §05) used only by the oracle's own
@@ -97,9 +100,21 @@ def row_scale(valid: np.ndarray, n_valid: int, reduction: str, grad_out) -> np.n
     return np.where(valid, s, 0.0)
 
 
-def _dlogits(X, Z, lse, labels, valid, scale, softcap):
+def _filter(P, labels, valid, filter_threshold):
+    """Gradient filtering: softmax entries below the threshold are dropped, except the
+    target entry of a valid row (Liger-CCE blog, §三: entries under 2^-12 vanish in the
+    bf16 gradient and are skipped).  threshold <= 0: nothing is dropped."""
+    if filter_threshold <= 0:
+        return P
+    keep = P >= filter_threshold
+    rows = np.nonzero(valid)[0]
+    keep[rows, np.asarray(labels)[rows]] = True
+    return np.where(keep, P, 0.0)
+
+
+def _dlogits(X, Z, lse, labels, valid, scale, softcap, filter_threshold=0.0):
     """dL/dx for a block of rows: (exp(z - lse) - onehot(y)) * scale * cap'(x)."""
-    P = np.exp(Z - lse[:, None])
+    P = _filter(np.exp(Z - lse[:, None]), labels, valid, filter_threshold)
     rows = np.nonzero(valid)[0]
     P[rows, np.asarray(labels)[rows]] -= 1.0
     return P * scale[:, None] * _cap_grad(X, softcap)
@@ -169,9 +184,10 @@ def target_rows(Hf, Wf, labels, rows, ignore_index: int = -100, softcap: float =
 
 # ----------------------------------------------------------------------------- backward
 def backward(Hf, Wf, labels, lse, ignore_index: int = -100, softcap: float = 0.0,
-             reduction: str = "mean", grad_out=1.0, row_block: int = 512):
+             reduction: str = "mean", grad_out=1.0, row_block: int = 512, filter_threshold: float = 0.0):
     """(dH, dW) from the saved per-row LSE.  dH sums over the vocabulary, dW over
-    the tokens; row blocks only bound memory."""
+    the tokens; row blocks only bound memory.  filter_threshold > 0 gives the
+    gradient of the filtered softmax (see _filter), an approximation of the exact one."""
     Hf = np.asarray(Hf, dtype=np.float64)
     Wf = np.asarray(Wf, dtype=np.float64)
     labels = np.asarray(labels, dtype=np.int64)
@@ -184,14 +200,15 @@ def backward(Hf, Wf, labels, lse, ignore_index: int = -100, softcap: float = 0.0
         r1 = min(N, r0 + row_block)
         X = _raw_logits(Hf[r0:r1], Wf)
         Z = _cap(X, softcap)
-        dX = _dlogits(X, Z, np.asarray(lse)[r0:r1], labels[r0:r1], valid[r0:r1], scale[r0:r1], softcap)
+        dX = _dlogits(X, Z, np.asarray(lse)[r0:r1], labels[r0:r1], valid[r0:r1], scale[r0:r1], softcap,
+                      filter_threshold)
         dH[r0:r1] = dX @ Wf
         dW += dX.T @ Hf[r0:r1]
     return dH, dW
 
 
 def dH_rows(Hf, Wf, labels, lse, rows, ignore_index=-100, softcap=0.0, reduction="mean",
-            grad_out=1.0, n_valid=None):
+            grad_out=1.0, n_valid=None, filter_threshold=0.0):
     """dH for selected rows.  `lse` holds the oracle's LSE of those rows; `n_valid`
     is the global valid count (needed by the mean reduction)."""
     Hf = np.asarray(Hf, np.float64)
@@ -206,12 +223,12 @@ def dH_rows(Hf, Wf, labels, lse, rows, ignore_index=-100, softcap=0.0, reduction
     scale = row_scale(valid, nv, reduction, g)
     X = _raw_logits(Hf[rows], Wf)
     Z = _cap(X, softcap)
-    dX = _dlogits(X, Z, np.asarray(lse, np.float64), labels[rows], valid, scale, softcap)
+    dX = _dlogits(X, Z, np.asarray(lse, np.float64), labels[rows], valid, scale, softcap, filter_threshold)
     return dX @ Wf
 
 
 def dW_rows(Hf, Wf, labels, lse_all, vocab, ignore_index=-100, softcap=0.0, reduction="mean",
-            grad_out=1.0):
+            grad_out=1.0, filter_threshold=0.0):
     """dW for selected vocabulary rows v: sum over every token of dZ_iv h_i.
     Needs the oracle's LSE of all N rows."""
     Hf = np.asarray(Hf, np.float64)
@@ -225,6 +242,8 @@ def dW_rows(Hf, Wf, labels, lse_all, vocab, ignore_index=-100, softcap=0.0, redu
     Z = _cap(X, softcap)
     P = np.exp(Z - np.asarray(lse_all, np.float64)[:, None])
     onehot = (labels[:, None] == vocab[None, :]) & valid[:, None]
+    if filter_threshold > 0:
+        P = np.where((P >= filter_threshold) | onehot, P, 0.0)
     dX = (P - onehot) * scale[:, None] * _cap_grad(X, softcap)
     return dX.T @ Hf
 

@@ -17,6 +17,10 @@ Recipes (one per workload; sizes follow the shapes the pages discuss):
               documents (3 distinct uniform cut points, every document >= 2 long),
               token ids Zipf(1.1); label[p] = token[p+1] inside a document and
               ignore_index at each document's last position; mean, seed 4.
+* ``peaked``  the llama3 shape with confident predictions: h_i = e_i + b w_{y_i} / |w_{y_i}|^2
+              (e_i ~ N(0,1), b = 14) for rows with a valid label, so the target logit
+              stands about 14 above the rest (p_y ~ 0.8, other entries mostly < 2^-12);
+              seed 5.  Used to measure gradient filtering.
 
 Random numbers come from the counter-based generator in ``synth.c`` (splitmix64 +
 Box-Muller), so a row range of H or W can be regenerated alone.
@@ -132,6 +136,7 @@ class Workload:
     n_seq: int = 0
     seq_len: int = 0
     n_docs: int = 0
+    peak: float = 0.0       # b of the peaked recipe (0: H is plain N(0,1))
     extra: dict = field(default_factory=dict)
 
     @property
@@ -150,6 +155,7 @@ WORKLOADS = {
     "gemma2": Workload("gemma2", 8192, 2304, 256128, 3, 0.02, "zipf", 0.05, softcap=30.0),
     "packed": Workload("packed", 32768, 3584, 152064, 4, 0.02, "packed", 0.0,
                        n_seq=8, seq_len=4096, n_docs=4),
+    "peaked": Workload("peaked", 8192, 4096, 128256, 5, 0.02, "zipf", 0.05, peak=14.0),
 }
 
 
@@ -209,9 +215,20 @@ def packed_labels(w: Workload) -> np.ndarray:
     return y
 
 
-def make_H(w: Workload, rows: slice | None = None) -> np.ndarray:
+def make_H(w: Workload, rows: slice | None = None, W: np.ndarray | None = None) -> np.ndarray:
+    """H rows [r0, r1) as bf16 bits.  For the peaked recipe the target direction is
+    added (W, the full bf16 weight, may be passed to avoid regenerating it)."""
     r0, r1 = (0, w.N) if rows is None else (rows.start, rows.stop)
-    return normal_bf16((r1 - r0, w.Hd), w.seed, STREAM_H, 1.0, offset=r0 * w.Hd)
+    e = normal_bf16((r1 - r0, w.Hd), w.seed, STREAM_H, 1.0, offset=r0 * w.Hd)
+    if w.peak <= 0:
+        return e
+    y = make_labels(w)[r0:r1]
+    ok = (y >= 0) & (y < w.V)
+    Wb = make_W(w) if W is None else W
+    wy = bf16_bits_to_f32(Wb[np.where(ok, y, 0)]).astype(np.float64)
+    h = bf16_bits_to_f32(e).astype(np.float64)
+    h[ok] += w.peak * wy[ok] / (wy[ok] ** 2).sum(axis=1, keepdims=True)
+    return f32_to_bf16_bits(h.astype(np.float32))
 
 
 def make_W(w: Workload, rows: slice | None = None) -> np.ndarray:
@@ -222,4 +239,5 @@ def make_W(w: Workload, rows: slice | None = None) -> np.ndarray:
 def make_inputs(w: Workload | str) -> dict:
     if isinstance(w, str):
         w = WORKLOADS[w]
-    return dict(H=make_H(w), W=make_W(w), labels=make_labels(w), workload=w)
+    Wb = make_W(w)
+    return dict(H=make_H(w, W=Wb), W=Wb, labels=make_labels(w), workload=w)

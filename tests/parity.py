@@ -37,14 +37,14 @@ def fro_rel(a: np.ndarray, ref: np.ndarray) -> float:
 
 
 def make_case(w: S.Workload, labels: np.ndarray | None = None):
-    Hb = S.make_H(w)
     Wb = S.make_W(w)
+    Hb = S.make_H(w, W=Wb)
     y = S.make_labels(w) if labels is None else labels
     return Hb, Wb, y
 
 
 def run_gpu(Hb, Wb, y, ignore_index=-100, softcap=0.0, reduction="mean", grad=None, chunk_budget=0,
-            backward=True):
+            backward=True, filter_threshold=0.0):
     import linear_cross_entropy_indexed_gb300 as F
     H = to_device(Hb)
     W = to_device(Wb)
@@ -57,7 +57,8 @@ def run_gpu(Hb, Wb, y, ignore_index=-100, softcap=0.0, reduction="mean", grad=No
         if grad is None:
             grad = np.linspace(0.5, 1.5, N) if reduction == "none" else np.array([1.0])
         g = torch.tensor(np.asarray(grad, dtype=np.float32)).cuda()
-        dH, dW = F.flce_backward(H, W, lab, lse, counts, g, ignore_index, softcap, reduction, chunk_budget)
+        dH, dW = F.flce_backward(H, W, lab, lse, counts, g, ignore_index, softcap, reduction, chunk_budget,
+                                 filter_threshold=filter_threshold)
         out["dH"] = S.bf16_bits_to_f32(bf16_bits(dH)).astype(np.float64)
         out["dW"] = S.bf16_bits_to_f32(bf16_bits(dW)).astype(np.float64)
         out["counts_after"] = counts.cpu().numpy()
@@ -100,7 +101,7 @@ def check_backward(out, dH_ref, dW_ref):
     return dict(dH_err=eh, dW_err=ew)
 
 
-def oracle_full(Hb, Wb, y, ignore_index=-100, softcap=0.0, reduction="mean", grad=None):
+def oracle_full(Hb, Wb, y, ignore_index=-100, softcap=0.0, reduction="mean", grad=None, filter_threshold=0.0):
     Hf = O.widen_bf16(Hb)
     Wf = O.widen_bf16(Wb)
     ref = O.forward(Hf, Wf, y, ignore_index, softcap, reduction)
@@ -110,5 +111,5 @@ def oracle_full(Hb, Wb, y, ignore_index=-100, softcap=0.0, reduction="mean", gra
     g = np.asarray(grad, dtype=np.float32).astype(np.float64)
     if reduction != "none":
         g = float(np.asarray(g).reshape(-1)[0])
-    dH, dW = O.backward(Hf, Wf, y, ref.lse, ignore_index, softcap, reduction, g)
+    dH, dW = O.backward(Hf, Wf, y, ref.lse, ignore_index, softcap, reduction, g, filter_threshold=filter_threshold)
     return ref, dH, dW

@@ -60,12 +60,14 @@ def test_workspace_sizes(lib):
     tiles = -(-v // 256)
     assert f(n, hd, v) >= 2 * (-(-tiles // 8)) * n * 4
     assert f(n, hd, v) < 2 * (-(-tiles // 4)) * n * 4 + (1 << 20)
-    # backward: one bf16 [N, Vc] chunk plus an fp32 [N, Hd] accumulator when chunked
+    # backward: one bf16 [N, Vc] chunk plus an fp32 [N, Hd] accumulator when chunked, and
+    # one byte per 64 x 64 block of the chunk for the filtered mode
     budget = 64 << 20
     vc = (budget // (2 * n)) // 256 * 256
     size = b(n, hd, v, budget)
-    assert size >= n * vc * 2 + n * hd * 4 + n * 16
-    assert size < n * vc * 2 + n * hd * 4 + n * 16 + (1 << 12)
+    flags = (n // 64) * (vc // 64)
+    assert size >= n * vc * 2 + n * hd * 4 + n * 16 + flags
+    assert size < n * vc * 2 + n * hd * 4 + n * 16 + flags + (1 << 12)
     # a single chunk needs no fp32 accumulator
     assert b(256, 64, 2000, 0) < 256 * 2048 * 2 + 256 * 16 + 4096
 
@@ -93,7 +95,8 @@ def test_argument_errors_before_any_device_work(lib):
     assert _fwd(lib, ws_bytes=16) == WS
     assert _fwd(lib, ws=0x10010) == WS
     assert _fwd(lib, N=1 << 40) == OVERFLOW
-    assert _bwd(lib, filt=0.5) == UNSUP
+    assert _bwd(lib, filt=-0.5) == ARG
+    assert _bwd(lib, filt=float("nan")) == ARG
     assert _bwd(lib, dW=None) == ARG
     assert _bwd(lib, ws_bytes=16) == WS
     assert _bwd(lib, W=0x2002) == ALIGN

@@ -340,8 +340,8 @@ def _mutants():
     def cap_grad_one(X, c):                    # dropped the softcap derivative
         return 1.0
 
-    def dl_wrong_sign(X, Z, lse, labels, valid, scale, c):  # +1 instead of -1 at the target
-        D = orig_dl(X, Z, lse, labels, valid, scale, c)
+    def dl_wrong_sign(X, Z, lse, labels, valid, scale, c, filt=0.0):  # +1 instead of -1 at the target
+        D = orig_dl(X, Z, lse, labels, valid, scale, c, filt)
         rows = np.nonzero(valid)[0]
         D[rows, np.asarray(labels)[rows]] += 2.0 * scale[rows] * np.asarray(orig_cap_grad(X, c) * np.ones_like(X))[rows, np.asarray(labels)[rows]]
         return D
@@ -374,3 +374,45 @@ def test_planted_mistake_is_caught(mutant, monkeypatch):
     name, fn = _mutants()[mutant]
     monkeypatch.setattr(O, name, fn)
     assert _caught() >= 1, name
+
+
+# ------------------------------------------------------------------ gradient filtering
+def test_filtered_backward_pins():
+    """threshold 0 is the exact gradient; a threshold above every probability keeps only
+    the target entries, whose closed form is dH_i = (p_iy - 1) s_i w_y and
+    dW_v = sum over rows with y_i = v of (p_iy - 1) s_i h_i; an intermediate threshold
+    drops exactly the entries below it (brute force)."""
+    H, W, y = _case(7, 5, 23, seed=51)
+    f = O.forward(H, W, y)
+    exact = O.backward(H, W, y, f.lse)
+    zero = O.backward(H, W, y, f.lse, filter_threshold=0.0)
+    np.testing.assert_array_equal(exact[0], zero[0])
+    np.testing.assert_array_equal(exact[1], zero[1])
+    valid = y != -100
+    nv = valid.sum()
+    dH, dW = O.backward(H, W, y, f.lse, filter_threshold=2.0)
+    eh = np.zeros_like(H)
+    ew = np.zeros_like(W)
+    for i in np.nonzero(valid)[0]:
+        py = math.exp(float(H[i] @ W[y[i]]) - f.lse[i])
+        eh[i] = (py - 1.0) / nv * W[y[i]]
+        ew[y[i]] += (py - 1.0) / nv * H[i]
+    np.testing.assert_allclose(dH, eh, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(dW, ew, rtol=1e-12, atol=1e-15)
+    thr = 0.05
+    P = np.exp(H @ W.T - f.lse[:, None])
+    D = np.zeros_like(P)
+    for i in range(len(y)):
+        if not valid[i]:
+            continue
+        for v in range(W.shape[0]):
+            keep = P[i, v] >= thr or v == y[i]
+            D[i, v] = ((P[i, v] if keep else 0.0) - (v == y[i])) / nv
+    dH2, dW2 = O.backward(H, W, y, f.lse, filter_threshold=thr)
+    np.testing.assert_allclose(dH2, D @ W, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(dW2, D.T @ H, rtol=1e-12, atol=1e-15)
+    rows = np.array([0, 3])
+    np.testing.assert_allclose(O.dH_rows(H, W, y, f.lse[rows], rows, filter_threshold=thr), dH2[rows], rtol=1e-12,
+                               atol=1e-15)
+    vs = np.array([0, 4, 22])
+    np.testing.assert_allclose(O.dW_rows(H, W, y, f.lse, vs, filter_threshold=thr), dW2[vs], rtol=1e-12, atol=1e-15)
