@@ -160,6 +160,14 @@ FLCE_API flce_status flce_forward_noalloc(const void* H, const void* W, const in
                                  float* loss, float* lse, float* target_logit, int64_t* counts,
                                  void* stream);
 
+/* Failure-detection self-test.  The pages have no counterpart: it checks the device-side
+ * bounded waits that keep a broken pipeline from hanging the GPU.  Launches one kernel
+ * whose thread waits, with the same bounded mbarrier wait the tensor-core kernels use
+ * (limit 2 s), on a barrier nothing arrives on.  When the stream reaches it,
+ * status_word[0] (device int64, zeroed first) holds FLCE_DEVERR_WAIT_TIMEOUT and the
+ * kernel has returned normally; the context stays usable. */
+FLCE_API flce_status flce_selftest_wait_timeout(int64_t* status_word, void* stream);
+
 /* Human-readable text for a flce_status value. */
 FLCE_API const char* flce_strerror(int status);
 
@@ -184,6 +192,7 @@ FLCE_API int flce_last_cuda_error(void);
 #define FLCE_KERNEL_DH 7          /* tensor-core dH += dZ W_chunk                      */
 #define FLCE_KERNEL_ZERO 8        /* zero fill (dW when N == 0)                        */
 #define FLCE_KERNEL_BLOCK_MASK 9  /* filtered backward: live K steps per dW / dH tile   */
+#define FLCE_KERNEL_SELFTEST 10   /* flce_selftest_wait_timeout                        */
 FLCE_API uint64_t flce_launch_count(void);
 FLCE_API int flce_set_event_sink(void* const* start_events, void* const* end_events, int* kernel_ids,
                         int capacity);

@@ -34,7 +34,7 @@ __all__ = [
 
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 KERNEL_NAMES = {0: "label_dot", 1: "linear_lse", 2: "lse_merge", 3: "reduce", 4: "bwd_prep",
-                5: "dz", 6: "dw", 7: "dh", 8: "zero", 9: "block_mask"}
+                5: "dz", 6: "dw", 7: "dh", 8: "zero", 9: "block_mask", 10: "selftest"}
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +71,8 @@ def library() -> ctypes.CDLL:
             lib.flce_set_event_sink.argtypes = [vp, vp, vp, i32]
             lib.flce_set_event_sink.restype = i32
             lib.flce_event_sink_used.restype = i32
+            lib.flce_selftest_wait_timeout.argtypes = [vp, vp]
+            lib.flce_selftest_wait_timeout.restype = i32
             _lib = lib
     return _lib
 

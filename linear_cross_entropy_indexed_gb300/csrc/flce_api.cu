@@ -9,9 +9,26 @@
 
 #include "flce.h"
 #include "internal.cuh"
+#include "ptx.cuh"
 #include "small_kernels.cuh"
 
 namespace flce {
+
+// One thread waits, with the same bounded wait the tensor-core kernels use, on an
+// mbarrier that nothing ever arrives on: after the limit it sets the error bit and the
+// kernel returns (nothing faults or hangs).
+__global__ void k_wait_timeout_selftest(unsigned long long* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, err);
+}
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -455,6 +472,22 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return FLCE_OK;
+}
+
+flce_status flce_selftest_wait_timeout(int64_t* status_word, void* stream) {
+  if (!status_word) return FLCE_ERR_ARG;
+  if (!aligned(status_word, 8)) return FLCE_ERR_ALIGN;
+  int sms = 0;
+  flce_status s = device_setup(&sms);
+  if (s != FLCE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(status_word, 0, sizeof(int64_t), st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch(FLCE_KERNEL_SELFTEST, st, [&] {
+    k_wait_timeout_selftest<<<1, 32, 0, st>>>(reinterpret_cast<unsigned long long*>(status_word));
+    return cudaGetLastError();
+  });
+  return e == cudaSuccess ? FLCE_OK : cuda_fail(e);
 }
 
 const char* flce_strerror(int status) {
