@@ -160,6 +160,47 @@ FLCE_API flce_status flce_forward_noalloc(const void* H, const void* W, const in
                                  float* loss, float* lse, float* target_logit, int64_t* counts,
                                  void* stream);
 
+/* ---------------------------------------------------------------- vocabulary sharding
+ * Vocabulary-parallel use (ai-infra-kb M011, §07: with the vocabulary split across ranks,
+ * the global max, the global sum of exponentials and the target logit must be combined,
+ * and dH gets a contribution from every shard; GPU CE post, §4.3).  Each rank holds the
+ * rows [v_offset, v_offset + V_shard) of a vocabulary of V_total and the same H and
+ * labels (labels are global ids).
+ *   1. flce_forward_shard: lse_shard[i] = log sum over this shard's rows of e^{z_iv};
+ *      target_shard[i] = z_{i,y_i} when y_i is one of this shard's rows, else 0;
+ *      counts as in flce_forward (validity against V_total).  Workspace:
+ *      flce_forward_workspace_size(N, Hd, V_shard).
+ *   2. gather lse_shard and target_shard of all shards, in shard order, into
+ *      [n_shards][N] arrays (e.g. an all-gather), then flce_merge_shards: global lse,
+ *      loss (reduction as in flce_forward) and counts, merged in a fixed shard order.
+ *   3. flce_backward_shard with the global lse and counts: dW_shard (bf16 [V_shard, Hd],
+ *      complete) and dH_partial (fp32 [N, Hd], this shard's sum over its rows); the
+ *      caller sums dH_partial over the shards (e.g. an all-reduce) and rounds as needed.
+ *      A row whose label lives in another shard is still a valid row here.
+ *      Workspace: flce_backward_workspace_size(N, Hd, V_shard, chunk_budget_bytes).
+ * v_offset < 0, V_shard <= 0 or v_offset + V_shard > V_total: FLCE_ERR_ARG. */
+FLCE_API flce_status flce_forward_shard(const void* H, const void* W_shard, const int64_t* labels,
+                               int64_t N, int64_t Hd, int64_t V_shard, int64_t v_offset,
+                               int64_t V_total, int64_t ignore_index, float softcap,
+                               float* lse_shard, float* target_shard, int64_t* counts,
+                               void* workspace, size_t workspace_bytes, void* stream);
+/* Bytes of scratch that flce_merge_shards needs. */
+FLCE_API size_t flce_merge_shards_workspace_size(int64_t N);
+/*   lse_parts, target_parts (device) fp32 [n_shards][N], shard order
+ *   loss (device) fp32 [1] (MEAN/SUM) or [N] (NONE); lse (device) fp32 [N] global;
+ *   counts (device) int64 [3] written as by flce_forward. */
+FLCE_API flce_status flce_merge_shards(const float* lse_parts, const float* target_parts, int64_t n_shards,
+                              const int64_t* labels, int64_t N, int64_t V_total, int64_t ignore_index,
+                              int reduction, float* loss, float* lse, int64_t* counts,
+                              void* workspace, size_t workspace_bytes, void* stream);
+FLCE_API flce_status flce_backward_shard(const void* H, const void* W_shard, const int64_t* labels,
+                                const float* lse, int64_t* counts, int64_t N, int64_t Hd,
+                                int64_t V_shard, int64_t v_offset, int64_t V_total,
+                                int64_t ignore_index, float softcap, int reduction,
+                                const float* grad_out, float filter_threshold,
+                                float* dH_partial, void* dW_shard, void* workspace,
+                                size_t workspace_bytes, size_t chunk_budget_bytes, void* stream);
+
 /* Failure-detection self-test.  The pages have no counterpart: it checks the device-side
  * bounded waits that keep a broken pipeline from hanging the GPU.  Launches one kernel
  * whose thread waits, with the same bounded mbarrier wait the tensor-core kernels use
@@ -193,6 +234,7 @@ FLCE_API int flce_last_cuda_error(void);
 #define FLCE_KERNEL_ZERO 8        /* zero fill (dW when N == 0)                        */
 #define FLCE_KERNEL_BLOCK_MASK 9  /* filtered backward: live K steps per dW / dH tile   */
 #define FLCE_KERNEL_SELFTEST 10   /* flce_selftest_wait_timeout                        */
+#define FLCE_KERNEL_SHARD_MERGE 11 /* vocabulary shards: fixed-order LSE / loss merge  */
 FLCE_API uint64_t flce_launch_count(void);
 FLCE_API int flce_set_event_sink(void* const* start_events, void* const* end_events, int* kernel_ids,
                         int capacity);

@@ -27,14 +27,15 @@ import torch
 from . import _build
 
 __all__ = [
-    "linear_cross_entropy", "flce_forward", "flce_backward", "forward_workspace_size",
+    "linear_cross_entropy", "flce_forward", "flce_backward", "flce_forward_shard", "flce_merge_shards",
+    "flce_backward_shard", "forward_workspace_size",
     "backward_workspace_size", "FlceError", "check_counts", "library", "launch_count",
     "EventSink", "KERNEL_NAMES",
 ]
 
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 KERNEL_NAMES = {0: "label_dot", 1: "linear_lse", 2: "lse_merge", 3: "reduce", 4: "bwd_prep",
-                5: "dz", 6: "dw", 7: "dh", 8: "zero", 9: "block_mask", 10: "selftest"}
+                5: "dz", 6: "dw", 7: "dh", 8: "zero", 9: "block_mask", 10: "selftest", 11: "shard_merge"}
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +72,15 @@ def library() -> ctypes.CDLL:
             lib.flce_set_event_sink.argtypes = [vp, vp, vp, i32]
             lib.flce_set_event_sink.restype = i32
             lib.flce_event_sink_used.restype = i32
+            lib.flce_forward_shard.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp, vp, vp, vp, sz, vp]
+            lib.flce_forward_shard.restype = i32
+            lib.flce_merge_shards_workspace_size.argtypes = [i64]
+            lib.flce_merge_shards_workspace_size.restype = sz
+            lib.flce_merge_shards.argtypes = [vp, vp, i64, vp, i64, i64, i64, i32, vp, vp, vp, vp, sz, vp]
+            lib.flce_merge_shards.restype = i32
+            lib.flce_backward_shard.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, i32, vp, f32,
+                                                vp, vp, vp, sz, sz, vp]
+            lib.flce_backward_shard.restype = i32
             lib.flce_selftest_wait_timeout.argtypes = [vp, vp]
             lib.flce_selftest_wait_timeout.restype = i32
             _lib = lib
@@ -173,6 +183,70 @@ def flce_backward(H, W, labels, lse, counts, grad_out, ignore_index: int = -100,
                                        ws.numel(),
                                        int(chunk_budget), _stream(dev)))
     return dH, dW
+
+
+# ----------------------------------------------------------------- vocabulary sharding
+def flce_forward_shard(H, W_shard, labels, v_offset: int, V_total: int, ignore_index: int = -100,
+                       softcap: float = 0.0, workspace=None):
+    """Forward over one vocabulary shard (W rows [v_offset, v_offset + V_shard) of V_total).
+    Returns (lse_shard, target_shard, counts); merge the shards with flce_merge_shards."""
+    _check_inputs(H, W_shard, labels)
+    N, Hd = H.shape
+    Vs = W_shard.shape[0]
+    dev = H.device
+    with torch.cuda.device(dev):
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+        tgt = torch.empty(N, dtype=torch.float32, device=dev)
+        counts = torch.empty(3, dtype=torch.int64, device=dev)
+        need = forward_workspace_size(N, Hd, Vs)
+        ws = workspace if workspace is not None else torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        _check(library().flce_forward_shard(_p(H), _p(W_shard), _p(labels), N, Hd, Vs, int(v_offset), int(V_total),
+                                            int(ignore_index), float(softcap), _p(lse), _p(tgt), _p(counts), _p(ws),
+                                            ws.numel(), _stream(dev)))
+    return lse, tgt, counts
+
+
+def flce_merge_shards(lse_parts, target_parts, labels, V_total: int, ignore_index: int = -100, reduction="mean"):
+    """Fixed-order merge of [n_shards, N] per-shard LSEs and target logits (shard order)
+    into (loss, global lse, counts)."""
+    red = _reduction(reduction)
+    lse_parts = lse_parts.float().contiguous()
+    target_parts = target_parts.float().contiguous()
+    R, N = lse_parts.shape
+    dev = lse_parts.device
+    with torch.cuda.device(dev):
+        loss = torch.empty(N if red == 2 else 1, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+        counts = torch.empty(3, dtype=torch.int64, device=dev)
+        need = int(library().flce_merge_shards_workspace_size(N))
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        _check(library().flce_merge_shards(_p(lse_parts), _p(target_parts), R, _p(labels), N, int(V_total),
+                                           int(ignore_index), red, _p(loss), _p(lse), _p(counts), _p(ws), ws.numel(),
+                                           _stream(dev)))
+    return (loss if red == 2 else loss[0]), lse, counts
+
+
+def flce_backward_shard(H, W_shard, labels, lse, counts, grad_out, v_offset: int, V_total: int,
+                        ignore_index: int = -100, softcap: float = 0.0, reduction="mean", chunk_budget: int = 0,
+                        filter_threshold: float = 0.0):
+    """Backward over one vocabulary shard from the global lse and counts.  Returns
+    (dH_partial fp32 [N, Hd], to be summed over the shards; dW_shard bf16)."""
+    _check_inputs(H, W_shard, labels)
+    red = _reduction(reduction)
+    N, Hd = H.shape
+    Vs = W_shard.shape[0]
+    dev = H.device
+    g = grad_out.to(device=dev, dtype=torch.float32).reshape(-1).contiguous()
+    with torch.cuda.device(dev):
+        dh = torch.empty(N, Hd, dtype=torch.float32, device=dev)
+        dw = torch.empty_like(W_shard)
+        need = backward_workspace_size(N, Hd, Vs, chunk_budget)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        _check(library().flce_backward_shard(_p(H), _p(W_shard), _p(labels), _p(lse), _p(counts), N, Hd, Vs,
+                                             int(v_offset), int(V_total), int(ignore_index), float(softcap), red,
+                                             _p(g), float(filter_threshold), _p(dh), _p(dw), _p(ws), ws.numel(),
+                                             int(chunk_budget), _stream(dev)))
+    return dh, dw
 
 
 def check_counts(counts) -> tuple[int, int]:

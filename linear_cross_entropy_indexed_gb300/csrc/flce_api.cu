@@ -255,34 +255,22 @@ flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, BwdPl
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
-}  // namespace flce
 
-using namespace flce;
-
-extern "C" {
-
-size_t flce_forward_workspace_size(int64_t N, int64_t Hd, int64_t V) {
-  FwdPlan p;
-  return plan_forward(N, Hd, V, kPlanPairs, &p) == FLCE_OK ? p.total : 0;
-}
-
-size_t flce_backward_workspace_size(int64_t N, int64_t Hd, int64_t V, size_t chunk_budget_bytes) {
-  BwdPlan p;
-  return plan_backward(N, Hd, V, chunk_budget_bytes, &p) == FLCE_OK ? p.total : 0;
-}
-
-flce_status flce_forward(const void* H, const void* W, const int64_t* labels, int64_t N, int64_t Hd, int64_t V,
-                         int64_t ignore_index, float softcap, int reduction, float* loss, float* lse,
-                         float* target_logit, int64_t* counts, void* workspace, size_t workspace_bytes,
-                         void* stream) {
-  if (reduction < 0 || reduction > 2 || softcap != softcap) return FLCE_ERR_ARG;
+// Forward over the weight rows [v_offset, v_offset + V) of a vocabulary of V_total
+// (v_offset = 0 and V_total = V without sharding).  reduction -1: no loss output (the
+// sharded forward, whose per-shard LSE and target logits are merged later).
+flce_status forward_impl(const void* H, const void* W, const int64_t* labels, int64_t N, int64_t Hd, int64_t V,
+                         int64_t v_offset, int64_t V_total, int64_t ignore_index, float softcap, int reduction,
+                         float* loss, float* lse, float* target_logit, int64_t* counts, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (reduction < -1 || reduction > 2 || softcap != softcap) return FLCE_ERR_ARG;
   FwdPlan pl;
   flce_status s = plan_forward(N, Hd, V, kPlanPairs, &pl);
   if (s != FLCE_OK) return s;
-  if (!W || !loss || !counts) return FLCE_ERR_ARG;
+  if (!W || (reduction >= 0 && !loss) || !counts) return FLCE_ERR_ARG;
   if (N > 0 && (!H || !labels || !lse || !workspace)) return FLCE_ERR_ARG;
   if (!aligned(W, 16) || (H && !aligned(H, 16)) || !aligned(counts, 8) || (labels && !aligned(labels, 8)) ||
-      !aligned(loss, 4) || (lse && !aligned(lse, 4)) || (target_logit && !aligned(target_logit, 4)))
+      (loss && !aligned(loss, 4)) || (lse && !aligned(lse, 4)) || (target_logit && !aligned(target_logit, 4)))
     return FLCE_ERR_ALIGN;
   if (N > 0 && (workspace_bytes < pl.total || !aligned(workspace, kAlign))) return FLCE_ERR_WORKSPACE;
   int sms = 0;
@@ -292,7 +280,8 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* labels, in
   cudaError_t e = cudaMemsetAsync(counts, 0, 3 * sizeof(int64_t), st);
   if (e != cudaSuccess) return cuda_fail(e);
   if (N == 0) {
-    if (reduction != FLCE_REDUCTION_NONE && (e = cudaMemsetAsync(loss, 0, sizeof(float), st)) != cudaSuccess)
+    if ((reduction == FLCE_REDUCTION_MEAN || reduction == FLCE_REDUCTION_SUM) &&
+        (e = cudaMemsetAsync(loss, 0, sizeof(float), st)) != cudaSuccess)
       return cuda_fail(e);
     return FLCE_OK;
   }
@@ -308,8 +297,8 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* labels, in
 
   // (1) label scan + indexed dot
   e = launch(FLCE_KERNEL_LABEL_DOT, st, [&] {
-    k_label_dot<<<pl.dot_blocks, 32 * kDotWarps, 0, st>>>(Hb, Wb, labels, N, Hd, V, ignore_index, softcap, t_ws,
-                                                          target_logit, blk_counts);
+    k_label_dot<<<pl.dot_blocks, 32 * kDotWarps, 0, st>>>(Hb, Wb, labels, N, Hd, V, v_offset, V_total,
+                                                          ignore_index, softcap, t_ws, target_logit, blk_counts);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e);
@@ -335,7 +324,7 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* labels, in
   float* loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : nullptr;
   e = launch(FLCE_KERNEL_LSE_MERGE, st, [&] {
     k_lse_merge<<<pl.merge_blocks, kMergeThreads, 0, st>>>(part_m, part_s, pl.n_groups * kEpiSplit, N, t_ws, labels,
-                                                           ignore_index, V, lse, loss_rows, sums);
+                                                           ignore_index, V_total, lse, loss_rows, sums);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e);
@@ -349,18 +338,23 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* labels, in
   return FLCE_OK;
 }
 
-flce_status flce_backward(const void* H, const void* W, const int64_t* labels, const float* lse, int64_t* counts,
-                          int64_t N, int64_t Hd, int64_t V, int64_t ignore_index, float softcap, int reduction,
-                          const float* grad_out, float filter_threshold, void* dH, void* dW, void* workspace,
-                          size_t workspace_bytes, size_t chunk_budget_bytes, void* stream) {
+// Backward over the weight rows [v_offset, v_offset + V) of a vocabulary of V_total, from
+// the global LSE.  dh_partial (sharded backward): dH is written there in fp32 as this
+// shard's partial sum over its vocabulary rows instead of as bf16 into dH.
+flce_status backward_impl(const void* H, const void* W, const int64_t* labels, const float* lse, int64_t* counts,
+                          int64_t N, int64_t Hd, int64_t V, int64_t v_offset, int64_t V_total, int64_t ignore_index,
+                          float softcap, int reduction, const float* grad_out, float filter_threshold, void* dH,
+                          float* dh_partial, void* dW, void* workspace, size_t workspace_bytes,
+                          size_t chunk_budget_bytes, void* stream) {
   if (reduction < 0 || reduction > 2 || softcap != softcap || !(filter_threshold >= 0.0f)) return FLCE_ERR_ARG;
   const bool filter = filter_threshold > 0.0f;
   BwdPlan pl;
   flce_status s = plan_backward(N, Hd, V, chunk_budget_bytes, &pl);
   if (s != FLCE_OK) return s;
   if (!W || !dW || !counts) return FLCE_ERR_ARG;
-  if (N > 0 && (!H || !labels || !lse || !grad_out || !dH || !workspace)) return FLCE_ERR_ARG;
+  if (N > 0 && (!H || !labels || !lse || !grad_out || (!dH && !dh_partial) || !workspace)) return FLCE_ERR_ARG;
   if (!aligned(W, 16) || !aligned(dW, 16) || (H && !aligned(H, 16)) || (dH && !aligned(dH, 16)) ||
+      (dh_partial && !aligned(dh_partial, 16)) ||
       !aligned(counts, 8) || (labels && !aligned(labels, 8)) || (lse && !aligned(lse, 4)) ||
       (grad_out && !aligned(grad_out, 4)))
     return FLCE_ERR_ALIGN;
@@ -386,7 +380,8 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
   unsigned long long* err = reinterpret_cast<unsigned long long*>(counts + 2);
 
   e = launch(FLCE_KERNEL_BWD_PREP, st, [&] {
-    k_bwd_prep<<<cdiv(N, 256), 256, 0, st>>>(labels, lse, counts, grad_out, reduction, N, V, ignore_index, rows);
+    k_bwd_prep<<<cdiv(N, 256), 256, 0, st>>>(labels, lse, counts, grad_out, reduction, N, V, v_offset, V_total,
+                                             ignore_index, rows);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e);
@@ -466,12 +461,129 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
       s6.kmask = dh_mask;
       s6.kmask_ld = pl.dh_mask_ld;
     }
-    EpiDhParams p6{N, Hd, dh32, static_cast<__nv_bfloat16*>(dH), c == 0, c == pl.n_chunks - 1};
+    EpiDhParams p6 = dh_partial != nullptr
+                         ? EpiDhParams{N, Hd, dh_partial, nullptr, c == 0, 0}
+                         : EpiDhParams{N, Hd, dh32, static_cast<__nv_bfloat16*>(dH), c == 0, c == pl.n_chunks - 1};
     e = launch(FLCE_KERNEL_DH, st,
                [&] { return launch_dh(tmDz_k, tmW_mn, s6, p6, err, pair_grid(s6.units, sms), st); });
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return FLCE_OK;
+}
+
+}  // namespace flce
+
+using namespace flce;
+
+extern "C" {
+
+size_t flce_forward_workspace_size(int64_t N, int64_t Hd, int64_t V) {
+  FwdPlan p;
+  return plan_forward(N, Hd, V, kPlanPairs, &p) == FLCE_OK ? p.total : 0;
+}
+
+size_t flce_backward_workspace_size(int64_t N, int64_t Hd, int64_t V, size_t chunk_budget_bytes) {
+  BwdPlan p;
+  return plan_backward(N, Hd, V, chunk_budget_bytes, &p) == FLCE_OK ? p.total : 0;
+}
+
+flce_status flce_forward(const void* H, const void* W, const int64_t* labels, int64_t N, int64_t Hd, int64_t V,
+                         int64_t ignore_index, float softcap, int reduction, float* loss, float* lse,
+                         float* target_logit, int64_t* counts, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  if (reduction < 0 || reduction > 2) return FLCE_ERR_ARG;
+  return forward_impl(H, W, labels, N, Hd, V, 0, V, ignore_index, softcap, reduction, loss, lse, target_logit, counts,
+                      workspace, workspace_bytes, stream);
+}
+
+flce_status flce_backward(const void* H, const void* W, const int64_t* labels, const float* lse, int64_t* counts,
+                          int64_t N, int64_t Hd, int64_t V, int64_t ignore_index, float softcap, int reduction,
+                          const float* grad_out, float filter_threshold, void* dH, void* dW, void* workspace,
+                          size_t workspace_bytes, size_t chunk_budget_bytes, void* stream) {
+  if (N > 0 && !dH) return FLCE_ERR_ARG;
+  return backward_impl(H, W, labels, lse, counts, N, Hd, V, 0, V, ignore_index, softcap, reduction, grad_out,
+                       filter_threshold, dH, nullptr, dW, workspace, workspace_bytes, chunk_budget_bytes, stream);
+}
+
+namespace {
+flce_status check_shard(int64_t V_shard, int64_t v_offset, int64_t V_total) {
+  if (V_shard <= 0 || v_offset < 0 || V_total <= 0) return FLCE_ERR_ARG;
+  if (V_total > (int64_t(1) << 31) - 512) return FLCE_ERR_OVERFLOW;
+  if (v_offset > V_total - V_shard) return FLCE_ERR_ARG;
+  return FLCE_OK;
+}
+}  // namespace
+
+flce_status flce_forward_shard(const void* H, const void* W_shard, const int64_t* labels, int64_t N, int64_t Hd,
+                               int64_t V_shard, int64_t v_offset, int64_t V_total, int64_t ignore_index,
+                               float softcap, float* lse_shard, float* target_shard, int64_t* counts,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  flce_status s = check_shard(V_shard, v_offset, V_total);
+  if (s != FLCE_OK) return s;
+  if (N > 0 && !target_shard) return FLCE_ERR_ARG;
+  return forward_impl(H, W_shard, labels, N, Hd, V_shard, v_offset, V_total, ignore_index, softcap, -1, nullptr,
+                      lse_shard, target_shard, counts, workspace, workspace_bytes, stream);
+}
+
+size_t flce_merge_shards_workspace_size(int64_t N) {
+  if (N < 0) return 0;
+  const size_t blocks = std::max(cdiv(N, kMergeThreads), 1);
+  return align_up(blocks * sizeof(double)) + align_up(blocks * sizeof(int2));
+}
+
+flce_status flce_merge_shards(const float* lse_parts, const float* target_parts, int64_t n_shards,
+                              const int64_t* labels, int64_t N, int64_t V_total, int64_t ignore_index, int reduction,
+                              float* loss, float* lse, int64_t* counts, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (reduction < 0 || reduction > 2 || n_shards <= 0 || n_shards > (int64_t(1) << 20) || N < 0 || V_total <= 0)
+    return FLCE_ERR_ARG;
+  if (!loss || !counts) return FLCE_ERR_ARG;
+  if (N > 0 && (!lse_parts || !target_parts || !labels || !lse || !workspace)) return FLCE_ERR_ARG;
+  if (!aligned(counts, 8) || !aligned(loss, 4) || (labels && !aligned(labels, 8))) return FLCE_ERR_ALIGN;
+  size_t total;
+  if (!mul_ok(size_t(n_shards), size_t(N), &total)) return FLCE_ERR_OVERFLOW;
+  const size_t need = flce_merge_shards_workspace_size(N);
+  if (N > 0 && (workspace_bytes < need || !aligned(workspace, kAlign))) return FLCE_ERR_WORKSPACE;
+  int sms = 0;
+  flce_status s = device_setup(&sms);
+  if (s != FLCE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(counts, 0, 3 * sizeof(int64_t), st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (N == 0) {
+    if (reduction != FLCE_REDUCTION_NONE && (e = cudaMemsetAsync(loss, 0, sizeof(float), st)) != cudaSuccess)
+      return cuda_fail(e);
+    return FLCE_OK;
+  }
+  const int blocks = std::max(cdiv(N, kMergeThreads), 1);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  double* sums = reinterpret_cast<double*>(ws);
+  int2* blk_counts = reinterpret_cast<int2*>(ws + align_up(size_t(blocks) * sizeof(double)));
+  float* loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : nullptr;
+  e = launch(FLCE_KERNEL_SHARD_MERGE, st, [&] {
+    k_shard_merge<<<blocks, kMergeThreads, 0, st>>>(lse_parts, target_parts, static_cast<int>(n_shards), N, labels,
+                                                    ignore_index, V_total, lse, loss_rows, sums, blk_counts);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch(FLCE_KERNEL_REDUCE, st, [&] {
+    k_reduce<<<1, 256, 0, st>>>(sums, blocks, blk_counts, blocks, reduction, loss, counts);
+    return cudaGetLastError();
+  });
+  return e == cudaSuccess ? FLCE_OK : cuda_fail(e);
+}
+
+flce_status flce_backward_shard(const void* H, const void* W_shard, const int64_t* labels, const float* lse,
+                                int64_t* counts, int64_t N, int64_t Hd, int64_t V_shard, int64_t v_offset,
+                                int64_t V_total, int64_t ignore_index, float softcap, int reduction,
+                                const float* grad_out, float filter_threshold, float* dH_partial, void* dW_shard,
+                                void* workspace, size_t workspace_bytes, size_t chunk_budget_bytes, void* stream) {
+  flce_status s = check_shard(V_shard, v_offset, V_total);
+  if (s != FLCE_OK) return s;
+  if (N > 0 && !dH_partial) return FLCE_ERR_ARG;
+  return backward_impl(H, W_shard, labels, lse, counts, N, Hd, V_shard, v_offset, V_total, ignore_index, softcap,
+                       reduction, grad_out, filter_threshold, nullptr, dH_partial, dW_shard, workspace,
+                       workspace_bytes, chunk_budget_bytes, stream);
 }
 
 flce_status flce_selftest_wait_timeout(int64_t* status_word, void* stream) {

@@ -15,15 +15,17 @@ __device__ __forceinline__ float softcap_exact(float x, float c) {
   return c > 0.0f ? c * tanhf(x / c) : x;
 }
 
-// Label scan + indexed dot: for every row i, valid_i = (y_i != ignore) && 0 <= y_i < V,
-// bad_i = (y_i != ignore) && !(0 <= y_i < V), and t_i = cap(h_i . w_{y_i}) for valid
-// rows (0 otherwise).  One warp per row, 16-byte loads, fp32 FMA, butterfly sum.
-// Per-block (n_valid, n_bad) go to blk_counts for the fixed-order final reduction.
+// Label scan + indexed dot: for every row i, valid_i = (y_i != ignore) && 0 <= y_i < V_total,
+// bad_i = (y_i != ignore) && !valid_i, and t_i = cap(h_i . w_{y_i - v_offset}) when the label
+// falls in this weight's rows [v_offset, v_offset + V) (0 otherwise).  Without vocabulary
+// sharding v_offset = 0 and V_total = V.  One warp per row, 16-byte loads, fp32 FMA,
+// butterfly sum.  Per-block (n_valid, n_bad) go to blk_counts for the fixed-order final
+// reduction.
 __global__ void __launch_bounds__(32 * kDotWarps)
     k_label_dot(const __nv_bfloat16* __restrict__ H, const __nv_bfloat16* __restrict__ W,
-                const int64_t* __restrict__ labels, int64_t N, int64_t Hd, int64_t V, int64_t ignore,
-                float softcap, float* __restrict__ t_ws, float* __restrict__ t_user,
-                int2* __restrict__ blk_counts) {
+                const int64_t* __restrict__ labels, int64_t N, int64_t Hd, int64_t V, int64_t v_offset,
+                int64_t V_total, int64_t ignore, float softcap, float* __restrict__ t_ws,
+                float* __restrict__ t_user, int2* __restrict__ blk_counts) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int n_valid = 0, n_bad = 0;
@@ -32,12 +34,14 @@ __global__ void __launch_bounds__(32 * kDotWarps)
        i += static_cast<int64_t>(gridDim.x) * kDotWarps) {
     const int64_t y = labels[i];
     const bool ignored = y == ignore;
-    const bool in_range = y >= 0 && y < V;
+    const bool in_range = y >= 0 && y < V_total;
     const bool valid = !ignored && in_range;
+    const int64_t yl = y - v_offset;
+    const bool local = valid && yl >= 0 && yl < V;
     float acc = 0.0f;
-    if (valid) {
+    if (local) {
       const uint4* hp = reinterpret_cast<const uint4*>(H + i * Hd);
-      const uint4* wp = reinterpret_cast<const uint4*>(W + y * Hd);
+      const uint4* wp = reinterpret_cast<const uint4*>(W + yl * Hd);
       for (int64_t k = lane; k < vec; k += 32) {
         const uint4 a = __ldg(hp + k);
         const uint4 b = __ldg(wp + k);
@@ -83,7 +87,7 @@ __global__ void __launch_bounds__(32 * kDotWarps)
 __global__ void __launch_bounds__(kMergeThreads)
     k_lse_merge(const float* __restrict__ part_m, const float* __restrict__ part_s, int n_groups,
                 int64_t N, const float* __restrict__ t, const int64_t* __restrict__ labels,
-                int64_t ignore, int64_t V, float* __restrict__ lse_out, float* __restrict__ loss_rows,
+                int64_t ignore, int64_t V_total, float* __restrict__ lse_out, float* __restrict__ loss_rows,
                 double* __restrict__ blk_sums) {
   __shared__ double sh[kMergeThreads];
   const int64_t i = static_cast<int64_t>(blockIdx.x) * kMergeThreads + threadIdx.x;
@@ -101,7 +105,7 @@ __global__ void __launch_bounds__(kMergeThreads)
     const float lse = (m + log2f(s)) * kLn2;
     lse_out[i] = lse;
     const int64_t y = labels[i];
-    const bool valid = y != ignore && y >= 0 && y < V;
+    const bool valid = y != ignore && y >= 0 && y < V_total;
     const float l = valid ? lse - t[i] : 0.0f;
     if (loss_rows) loss_rows[i] = l;
     mine = l;
@@ -149,14 +153,17 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// Backward per-row data: scale_i (0 for ignored rows), label (or -1), lse * log2 e.
+// Backward per-row data: scale_i (0 for ignored rows), the label as a row of this weight
+// (-1 when ignored or, with vocabulary sharding, held by another shard), lse * log2 e.
 __global__ void k_bwd_prep(const int64_t* __restrict__ labels, const float* __restrict__ lse,
                            const int64_t* __restrict__ counts, const float* __restrict__ grad,
-                           int reduction, int64_t N, int64_t V, int64_t ignore, RowInfo* __restrict__ out) {
+                           int reduction, int64_t N, int64_t V, int64_t v_offset, int64_t V_total, int64_t ignore,
+                           RowInfo* __restrict__ out) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= N) return;
   const int64_t y = labels[i];
-  const bool valid = y != ignore && y >= 0 && y < V;
+  const bool valid = y != ignore && y >= 0 && y < V_total;
+  const int64_t yl = y - v_offset;
   float scale = 0.0f;
   if (valid) {
     if (reduction == 0) {
@@ -171,9 +178,59 @@ __global__ void k_bwd_prep(const int64_t* __restrict__ labels, const float* __re
   RowInfo r;
   r.lse2 = lse[i] * kLog2e;
   r.scale = scale;
-  r.label = valid ? static_cast<int32_t>(y) : -1;
+  r.label = (valid && yl >= 0 && yl < V) ? static_cast<int32_t>(yl) : -1;
   r.pad = 0;
   out[i] = r;
+}
+
+// Vocabulary-sharded forward: fixed-order merge (shard 0, 1, ...) of the per-shard row
+// LSEs into the global one, lse = m + log sum_r exp(lse_r - m), the target logit as the
+// sum of the per-shard ones (exactly one shard holds it), the per-row loss, and
+// per-block loss sums (double) and (n_valid, n_bad) counts.
+__global__ void __launch_bounds__(kMergeThreads)
+    k_shard_merge(const float* __restrict__ lse_parts, const float* __restrict__ t_parts, int n_shards, int64_t N,
+                  const int64_t* __restrict__ labels, int64_t ignore, int64_t V_total, float* __restrict__ lse_out,
+                  float* __restrict__ loss_rows, double* __restrict__ blk_sums, int2* __restrict__ blk_counts) {
+  __shared__ double sh[kMergeThreads];
+  __shared__ int sv[kMergeThreads], sb[kMergeThreads];
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kMergeThreads + threadIdx.x;
+  double mine = 0.0;
+  int v = 0, b = 0;
+  if (i < N) {
+    float m = -INFINITY;
+    for (int r = 0; r < n_shards; ++r) m = fmaxf(m, lse_parts[static_cast<int64_t>(r) * N + i]);
+    float s = 0.0f, t = 0.0f;
+    for (int r = 0; r < n_shards; ++r) {
+      s += expf(lse_parts[static_cast<int64_t>(r) * N + i] - m);
+      t += t_parts[static_cast<int64_t>(r) * N + i];
+    }
+    const float lse = m + logf(s);
+    lse_out[i] = lse;
+    const int64_t y = labels[i];
+    const bool ignored = y == ignore;
+    const bool valid = !ignored && y >= 0 && y < V_total;
+    const float l = valid ? lse - t : 0.0f;
+    if (loss_rows) loss_rows[i] = l;
+    mine = l;
+    v = valid ? 1 : 0;
+    b = (!ignored && !valid) ? 1 : 0;
+  }
+  sh[threadIdx.x] = mine;
+  sv[threadIdx.x] = v;
+  sb[threadIdx.x] = b;
+  __syncthreads();
+  for (int w = kMergeThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      sh[threadIdx.x] += sh[threadIdx.x + w];
+      sv[threadIdx.x] += sv[threadIdx.x + w];
+      sb[threadIdx.x] += sb[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    blk_sums[blockIdx.x] = sh[0];
+    blk_counts[blockIdx.x] = make_int2(sv[0], sb[0]);
+  }
 }
 
 // Bitmasks of the live K steps of the dW and dH products over a filtered dZ chunk.

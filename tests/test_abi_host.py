@@ -102,6 +102,22 @@ def test_argument_errors_before_any_device_work(lib):
     assert _bwd(lib, W=0x2002) == ALIGN
 
 
+def test_shard_argument_errors(lib):
+    f = lambda vs, off, vt: lib.flce_forward_shard(0x1000, 0x2000, 0x3000, 16, 64, vs, off, vt, -100, 0.0, 0x5000,
+                                                   0x5400, 0x6000, 0x10000, 1 << 20, None)
+    assert f(100, -1, 300) == ARG
+    assert f(100, 250, 300) == ARG
+    assert f(0, 0, 300) == ARG
+    assert f(100, 0, 1 << 40) == OVERFLOW
+    b = lambda off, vt: lib.flce_backward_shard(0x1000, 0x2000, 0x3000, 0x5000, 0x6000, 16, 64, 100, off, vt, -100,
+                                                0.0, 0, 0x8000, 0.0, 0x9000, 0x7000, 0x10000, 1 << 24, 0, None)
+    assert b(-5, 300) == ARG and b(201, 300) == ARG
+    m = lambda n, red: lib.flce_merge_shards(0x1000, 0x2000, n, 0x3000, 16, 300, -100, red, 0x4000, 0x5000, 0x6000,
+                                             0x10000, 1 << 20, None)
+    assert m(0, 0) == ARG and m(2, 5) == ARG
+    assert lib.flce_merge_shards_workspace_size(1000) > 0
+
+
 def test_valid_arguments_without_a_device_fail_cleanly(lib):
     # Arguments pass the checks; without a GPU the first CUDA call fails and the
     # library reports FLCE_ERR_CUDA (nothing is dereferenced on the host).
