@@ -27,7 +27,7 @@ import torch
 from . import _build
 
 __all__ = [
-    "linear_cross_entropy", "flce_forward", "flce_backward", "flce_forward_shard", "flce_merge_shards",
+    "linear_cross_entropy", "FusedLinearCrossEntropyLoss", "flce_forward", "flce_backward", "flce_forward_shard", "flce_merge_shards",
     "flce_backward_shard", "forward_workspace_size",
     "backward_workspace_size", "FlceError", "check_counts", "library", "launch_count",
     "EventSink", "KERNEL_NAMES",
@@ -292,6 +292,35 @@ def linear_cross_entropy(hidden, weight, labels, ignore_index: int = -100, softc
     if reduction == "none":
         out = out.reshape(labels.shape)
     return out
+
+
+class FusedLinearCrossEntropyLoss(torch.nn.Module):
+    """Module form of :func:`linear_cross_entropy`.
+
+    ``forward(weight, hidden, labels)`` takes the LM-head weight first, the argument
+    order of Liger's fused linear cross-entropy loss (Liger-CCE blog, §四); use
+    :func:`linear_cross_entropy` for the hidden-first order of CCE's
+    ``linear_cross_entropy(hidden, weight, labels)``.  Labels must already be shifted
+    for next-token prediction.
+    """
+
+    def __init__(self, ignore_index: int = -100, softcap: float = 0.0, reduction: str = "mean",
+                 chunk_budget: int = 0, filter_threshold: float = 0.0):
+        super().__init__()
+        _reduction(reduction)
+        self.ignore_index = int(ignore_index)
+        self.softcap = float(softcap)
+        self.reduction = reduction
+        self.chunk_budget = int(chunk_budget)
+        self.filter_threshold = float(filter_threshold)
+
+    def forward(self, weight, hidden, labels):
+        return linear_cross_entropy(hidden, weight, labels, self.ignore_index, self.softcap, self.reduction,
+                                    self.chunk_budget, self.filter_threshold)
+
+    def extra_repr(self):
+        return "ignore_index=%d, softcap=%g, reduction=%s, filter_threshold=%g" % (
+            self.ignore_index, self.softcap, self.reduction, self.filter_threshold)
 
 
 def launch_count() -> int:

@@ -1,0 +1,86 @@
+"""User-facing API on the GPU: the module form, argument checks of the binding, and a
+whole forward + backward step captured in a CUDA graph and replayed."""
+import numpy as np
+import pytest
+import torch
+
+import synthetic as S
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+def test_module_matches_function_and_oracle():
+    import linear_cross_entropy_indexed_gb300 as F
+    w = S.scaled("gemma2", N=200, Hd=96, V=1500, seed=81, w_std=0.3)
+    Hb, Wb, y = P.make_case(w)
+    H = P.to_device(Hb).requires_grad_(True)
+    W = P.to_device(Wb).requires_grad_(True)
+    lab = torch.from_numpy(y).cuda()
+    m = F.FusedLinearCrossEntropyLoss(softcap=w.softcap)
+    loss = m(W, H, lab)
+    loss.backward()
+    ref, dH, dW = P.oracle_full(Hb, Wb, y, softcap=w.softcap)
+    assert abs(loss.item() - float(ref.loss)) <= P.TOL_LOSS_REL * float(ref.loss)
+    gh = S.bf16_bits_to_f32(P.bf16_bits(H.grad)).astype(np.float64)
+    gw = S.bf16_bits_to_f32(P.bf16_bits(W.grad)).astype(np.float64)
+    assert P.fro_rel(gh, dH) <= P.TOL_GRAD_FRO and P.fro_rel(gw, dW) <= P.TOL_GRAD_FRO
+    assert "softcap=30" in repr(m)
+
+
+def test_binding_rejects_bad_inputs():
+    import linear_cross_entropy_indexed_gb300 as F
+    H = torch.zeros(4, 64, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(10, 64, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(4, dtype=torch.int64, device="cuda")
+    with pytest.raises(F.FlceError):
+        F.flce_forward(H.float(), W, y)
+    with pytest.raises(F.FlceError):
+        F.flce_forward(H, W[:, :32], y)
+    with pytest.raises(F.FlceError):
+        F.flce_forward(H, W, y.int())
+    with pytest.raises(F.FlceError):
+        F.flce_forward(H[:, :60], W[:, :60], y)  # hidden size not a multiple of 8
+    with pytest.raises(ValueError):
+        F.flce_forward(H, W, y, reduction="avg")
+    y[0] = 10
+    loss, lse, counts, _ = F.flce_forward(H, W, y)
+    with pytest.raises(F.FlceError):
+        F.check_counts(counts)  # one label outside [0, V)
+
+
+def test_step_captured_in_a_cuda_graph():
+    """Forward + backward through the C ABI captured once and replayed: the library
+    neither allocates nor synchronises, so the graph replays the same kernels."""
+    import linear_cross_entropy_indexed_gb300 as F
+    w = S.scaled("llama2", N=384, Hd=128, V=3000, seed=82, w_std=0.05)
+    Hb, Wb, y = P.make_case(w)
+    H, W = P.to_device(Hb), P.to_device(Wb)
+    lab = torch.from_numpy(y).cuda()
+    N, Hd, V = 384, 128, 3000
+    budget = 384 * 2 * 1024
+    ws = torch.empty(max(F.forward_workspace_size(N, Hd, V), F.backward_workspace_size(N, Hd, V, budget)),
+                     dtype=torch.uint8, device="cuda")
+    dH = torch.empty_like(H)
+    dW = torch.empty_like(W)
+    g = torch.ones(1, device="cuda")
+    # eager reference and warm-up (device setup happens on the first call)
+    loss_e, lse_e, counts_e, _ = F.flce_forward(H, W, lab, workspace=ws)
+    F.flce_backward(H, W, lab, lse_e, counts_e, g, chunk_budget=budget, workspace=ws, dH=dH, dW=dW)
+    torch.cuda.synchronize()
+    dH_e, dW_e, loss_eager = dH.clone(), dW.clone(), loss_e.item()
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            loss_g, lse_g, counts_g, _ = F.flce_forward(H, W, lab, workspace=ws)
+            F.flce_backward(H, W, lab, lse_g, counts_g, g, chunk_budget=budget, workspace=ws, dH=dH, dW=dW)
+    torch.cuda.current_stream().wait_stream(stream)
+    dH.zero_()
+    dW.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert loss_g.item() == loss_eager
+    assert torch.equal(dH, dH_e) and torch.equal(dW, dW_e)
