@@ -242,7 +242,9 @@ def run_ours(args, w):
         return loss, counts
 
     for _ in range(args.warmup):
+        n0 = F.launch_count()
         loss, counts = step()
+        launches_per_step = F.launch_count() - n0
     torch.cuda.synchronize()
     F.check_counts(counts)
 
@@ -250,7 +252,7 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     n_launch0 = F.launch_count()
     per_step = None
-    sink = F.EventSink(capacity=args.steps * 200)
+    sink = F.EventSink(capacity=args.steps * launches_per_step + 16)
     with ClockSampler(dev.index) as clk:
         if ws > 1:
             torch.distributed.barrier()
@@ -266,6 +268,8 @@ def run_ours(args, w):
         if ws > 1:
             torch.distributed.barrier()
     launches = F.launch_count() - n_launch0
+    if sink.used < launches:
+        raise RuntimeError("event sink overflow: %d of %d launches recorded" % (sink.used, launches))
     ms = e0.elapsed_time(e1) / args.steps
     if ws > 1:
         t = torch.tensor([ms], device=dev)
