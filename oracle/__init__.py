@@ -29,6 +29,10 @@ What it computes is the plain definition, row by row, in double precision:
 * filtering     optionally, softmax entries below a threshold (other than a valid row's
                 target) are dropped before forming dZ: CCE's gradient filtering
                 (Liger-CCE blog, §三), an approximation of the exact gradient
+* vocab order   the sort key of each vocabulary entry (its raw logit averaged over the
+                batch's rows) and the order that puts high keys first (Liger-CCE blog,
+                §三: the forward tallies each word's mean logit and the backward places
+                the frequent words in neighbouring blocks so that skipping is block-aligned)
 
 ``forward_split`` is a blockwise restatement (row chunks x vocab chunks merged with
 the running (m, s) rule of ai-infra-kb M011 §05) used only by the oracle's own
@@ -249,6 +253,26 @@ def dW_rows(Hf, Wf, labels, lse_all, vocab, ignore_index=-100, softcap=0.0, redu
 
 
 # ----------------------------------------------------------------------------- blockwise
+# ------------------------------------------------------------------ vocabulary order
+def vocab_keys(Hf, Wf, vocab=None) -> np.ndarray:
+    """Sort key of each vocabulary entry v: (1/N) sum_i x_iv, the raw logit h_i . w_v
+    (before any softcap) averaged over all N rows, ignored rows included; 0 when N = 0
+    (Liger-CCE blog, §三, the forward's per-word mean logit; which logit and which rows
+    is a reading, the pages name neither).  ``vocab`` restricts the output to those ids."""
+    Ws = Wf if vocab is None else Wf[np.asarray(vocab)]
+    if Hf.shape[0] == 0:
+        return np.zeros(Ws.shape[0])
+    return _raw_logits(Hf, Ws).mean(axis=0)
+
+
+def vocab_order(keys) -> np.ndarray:
+    """The sorted vocabulary as a permutation: perm[p] is the id placed at position p.
+    Keys descending (the frequent, high-logit words first); equal keys keep ascending
+    id order, so the permutation is unique (Liger-CCE blog, §三)."""
+    k = np.asarray(keys, dtype=np.float64)
+    return np.lexsort((np.arange(k.size), -k)).astype(np.int64)
+
+
 def merge(m1, s1, m2, s2):
     """Merge two (running max, scaled sum) pairs: m' = max(m1, m2),
     s' = s1 e^{m1-m'} + s2 e^{m2-m'}.  A side that has seen nothing (m = -inf, s = 0)

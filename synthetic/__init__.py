@@ -21,6 +21,14 @@ Recipes (one per workload; sizes follow the shapes the pages discuss):
               (e_i ~ N(0,1), b = 14) for rows with a valid label, so the target logit
               stands about 14 above the rest (p_y ~ 0.8, other entries mostly < 2^-12);
               seed 5.  Used to measure gradient filtering.
+* ``unigram`` the llama3 shape with a unigram prior, standing in for a trained model whose
+              logits favour frequent words: feature 0 of every hidden state is 1 and
+              feature 0 of w_v is -1.1 ln(rank(v) + 1), rank(v) being v's rank in the
+              label draw, so softmax of the prior alone is the labels' own Zipf(1.1) law;
+              the other features are the peaked recipe with b = 8 (applied to features
+              1..Hd-1 only).  About 1e-3 of the softmax entries exceed 2^-12, mostly the
+              frequent words, scattered over the ids by the rank permutation; seed 6.
+              Used to measure vocabulary sorting.
 
 Random numbers come from the counter-based generator in ``synth.c`` (splitmix64 +
 Box-Muller), so a row range of H or W can be regenerated alone.
@@ -137,6 +145,7 @@ class Workload:
     seq_len: int = 0
     n_docs: int = 0
     peak: float = 0.0       # b of the peaked recipe (0: H is plain N(0,1))
+    unigram: float = 0.0    # slope of the unigram prior in feature 0 (0: none)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -156,6 +165,7 @@ WORKLOADS = {
     "packed": Workload("packed", 32768, 3584, 152064, 4, 0.02, "packed", 0.0,
                        n_seq=8, seq_len=4096, n_docs=4),
     "peaked": Workload("peaked", 8192, 4096, 128256, 5, 0.02, "zipf", 0.05, peak=14.0),
+    "unigram": Workload("unigram", 8192, 4096, 128256, 6, 0.02, "zipf", 0.05, peak=8.0, unigram=1.1),
 }
 
 
@@ -217,23 +227,39 @@ def packed_labels(w: Workload) -> np.ndarray:
 
 def make_H(w: Workload, rows: slice | None = None, W: np.ndarray | None = None) -> np.ndarray:
     """H rows [r0, r1) as bf16 bits.  For the peaked recipe the target direction is
-    added (W, the full bf16 weight, may be passed to avoid regenerating it)."""
+    added (W, the full bf16 weight, may be passed to avoid regenerating it); with the
+    unigram prior feature 0 is set to 1 and carries no part of that direction."""
     r0, r1 = (0, w.N) if rows is None else (rows.start, rows.stop)
     e = normal_bf16((r1 - r0, w.Hd), w.seed, STREAM_H, 1.0, offset=r0 * w.Hd)
-    if w.peak <= 0:
+    if w.peak <= 0 and w.unigram <= 0:
         return e
-    y = make_labels(w)[r0:r1]
-    ok = (y >= 0) & (y < w.V)
-    Wb = make_W(w) if W is None else W
-    wy = bf16_bits_to_f32(Wb[np.where(ok, y, 0)]).astype(np.float64)
     h = bf16_bits_to_f32(e).astype(np.float64)
-    h[ok] += w.peak * wy[ok] / (wy[ok] ** 2).sum(axis=1, keepdims=True)
+    if w.peak > 0:
+        y = make_labels(w)[r0:r1]
+        ok = (y >= 0) & (y < w.V)
+        Wb = make_W(w) if W is None else W
+        wy = bf16_bits_to_f32(Wb[np.where(ok, y, 0)]).astype(np.float64)
+        if w.unigram > 0:
+            wy[:, 0] = 0.0
+        h[ok] += w.peak * wy[ok] / (wy[ok] ** 2).sum(axis=1, keepdims=True)
+    if w.unigram > 0:
+        h[:, 0] = 1.0
     return f32_to_bf16_bits(h.astype(np.float32))
+
+
+def unigram_prior(w: Workload) -> np.ndarray:
+    """-s ln(rank(v) + 1) for every id v, rank(v) its rank in the Zipf label draw."""
+    rank = np.empty(w.V, dtype=np.int64)
+    rank[permutation(w.V, w.seed)] = np.arange(w.V)
+    return -w.unigram * np.log(rank + 1.0)
 
 
 def make_W(w: Workload, rows: slice | None = None) -> np.ndarray:
     r0, r1 = (0, w.V) if rows is None else (rows.start, rows.stop)
-    return normal_bf16((r1 - r0, w.Hd), w.seed, STREAM_W, w.w_std, offset=r0 * w.Hd)
+    Wb = normal_bf16((r1 - r0, w.Hd), w.seed, STREAM_W, w.w_std, offset=r0 * w.Hd)
+    if w.unigram > 0:
+        Wb[:, 0] = f32_to_bf16_bits(unigram_prior(w)[r0:r1].astype(np.float32))
+    return Wb
 
 
 def make_inputs(w: Workload | str) -> dict:

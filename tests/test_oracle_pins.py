@@ -416,3 +416,63 @@ def test_filtered_backward_pins():
                                atol=1e-15)
     vs = np.array([0, 4, 22])
     np.testing.assert_allclose(O.dW_rows(H, W, y, f.lse, vs, filter_threshold=thr), dW2[vs], rtol=1e-12, atol=1e-15)
+
+
+# ------------------------------------------------------------------ vocabulary order
+def _order_by_selection(keys):
+    """Brute force: repeatedly take the largest remaining key, the smallest id on ties."""
+    left = list(range(len(keys)))
+    out = []
+    while left:
+        best = left[0]
+        for v in left[1:]:
+            if keys[v] > keys[best]:
+                best = v
+        out.append(best)
+        left.remove(best)
+    return out
+
+
+def test_vocab_order_pins():
+    """Hand-worked case: H = [[1, 0], [3, 2]], W rows (1,1), (0,2), (2,0), (1,1) give the
+    logits [[1, 0, 2, 1], [5, 4, 6, 5]], mean logits [3, 2, 4, 3] and the order
+    [2, 0, 3, 1] (ids 0 and 3 tie at 3 and keep id order)."""
+    H = np.array([[1.0, 0.0], [3.0, 2.0]])
+    W = np.array([[1.0, 1.0], [0.0, 2.0], [2.0, 0.0], [1.0, 1.0]])
+    keys = O.vocab_keys(H, W)
+    np.testing.assert_array_equal(keys, [3.0, 2.0, 4.0, 3.0])
+    assert O.vocab_order(keys).tolist() == [2, 0, 3, 1]
+    np.testing.assert_array_equal(O.vocab_keys(H, W, vocab=[3, 1]), [3.0, 2.0])
+    # ties and stability
+    assert O.vocab_order([1.0, 5.0, 5.0, -2.0, 5.0, 0.0]).tolist() == [1, 2, 4, 0, 5, 3]
+    assert O.vocab_order([0.0, -0.0, 0.0]).tolist() == [0, 1, 2]
+    # brute force on random keys with many ties
+    rng = np.random.default_rng(61)
+    for n in (1, 2, 17, 64):
+        k = np.round(rng.standard_normal(n) * 2.0) / 2.0
+        assert O.vocab_order(k).tolist() == _order_by_selection(list(k))
+    # closed form: a constant first feature and nothing else makes the key that column
+    Hc = np.zeros((9, 4))
+    Hc[:, 0] = 1.0
+    Wc = rng.standard_normal((11, 4))
+    np.testing.assert_allclose(O.vocab_keys(Hc, Wc), Wc[:, 0], rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(O.vocab_keys(np.zeros((0, 4)), Wc), np.zeros(11))
+    # the mean over rows, brute force on a small random case
+    Hr, Wr = rng.standard_normal((5, 3)), rng.standard_normal((7, 3))
+    brute = [sum(sum(Hr[i, k] * Wr[v, k] for k in range(3)) for i in range(5)) / 5 for v in range(7)]
+    np.testing.assert_allclose(O.vocab_keys(Hr, Wr), brute, rtol=1e-13, atol=1e-15)
+
+
+@pytest.mark.parametrize("mutant", ["ascending", "ties_descending", "sum_not_mean", "mean_over_vocab"])
+def test_vocab_order_mistake_is_caught(mutant, monkeypatch):
+    orig_keys = O.vocab_keys
+    if mutant == "ascending":
+        monkeypatch.setattr(O, "vocab_order", lambda k: np.lexsort((np.arange(len(k)), np.asarray(k, float))))
+    elif mutant == "ties_descending":
+        monkeypatch.setattr(O, "vocab_order", lambda k: np.lexsort((-np.arange(len(k)), -np.asarray(k, float))))
+    elif mutant == "sum_not_mean":
+        monkeypatch.setattr(O, "vocab_keys", lambda H, W, vocab=None: orig_keys(H, W, vocab) * max(H.shape[0], 1))
+    else:
+        monkeypatch.setattr(O, "vocab_keys", lambda H, W, vocab=None: (H @ W.T).mean(axis=1))  # over vocab
+    with pytest.raises((AssertionError, ValueError, IndexError)):
+        test_vocab_order_pins()
