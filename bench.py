@@ -134,6 +134,10 @@ def workload_desc(w) -> str:
     s = "%s: N=%d tokens, Hd=%d, V=%d, labels %s" % (w.name, w.N, w.Hd, w.V, w.labels)
     if w.softcap > 0:
         s += ", softcap %.1f" % w.softcap
+    if w.peak > 0:
+        s += ", target logit raised by %g" % w.peak
+    if w.unigram > 0:
+        s += ", unigram prior slope %g" % w.unigram
     return s
 
 
@@ -229,7 +233,8 @@ def run_ours(args, w):
     N, Hd, V = w.N, w.Hd, w.V
     red = w.reduction
     budget = args.chunk_budget
-    ws_bytes = max(F.forward_workspace_size(N, Hd, V), F.backward_workspace_size(N, Hd, V, budget))
+    ws_bytes = max(F.forward_workspace_size(N, Hd, V),
+                   F.backward_workspace_size(N, Hd, V, budget, args.sort_vocab))
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     dH = torch.empty_like(H)
     dW = torch.empty_like(W)
@@ -238,7 +243,7 @@ def run_ours(args, w):
     def step():
         loss, lse, counts, _ = F.flce_forward(H, W, y, w.ignore_index, w.softcap, red, workspace=workspace)
         F.flce_backward(H, W, y, lse, counts, g, w.ignore_index, w.softcap, red, budget, workspace=workspace,
-                        dH=dH, dW=dW, filter_threshold=args.filter_threshold)
+                        dH=dH, dW=dW, filter_threshold=args.filter_threshold, sort_vocab=args.sort_vocab)
         return loss, counts
 
     for _ in range(args.warmup):
@@ -332,7 +337,8 @@ def run_ours(args, w):
             cur.wait_event(copied[i % 2])
             Hx = b[0].detach().requires_grad_(True)
             Wx = b[1].detach().requires_grad_(True)
-            loss = F.linear_cross_entropy(Hx, Wx, b[2], w.ignore_index, w.softcap, red, budget, args.filter_threshold)
+            loss = F.linear_cross_entropy(Hx, Wx, b[2], w.ignore_index, w.softcap, red, budget, args.filter_threshold,
+                                          args.sort_vocab)
             loss.backward()
             freed[i % 2].record(cur)
             used[i % 2] = True
@@ -375,7 +381,8 @@ def run_ours(args, w):
     Wx = W.detach().requires_grad_(True)
     torch.cuda.reset_peak_memory_stats(dev)
     base = torch.cuda.memory_allocated(dev)
-    loss = F.linear_cross_entropy(Hx, Wx, y, w.ignore_index, w.softcap, red, budget, args.filter_threshold)
+    loss = F.linear_cross_entropy(Hx, Wx, y, w.ignore_index, w.softcap, red, budget, args.filter_threshold,
+                                  args.sort_vocab)
     loss.backward()
     torch.cuda.synchronize()
     peak = torch.cuda.max_memory_allocated(dev) - base
@@ -395,7 +402,7 @@ def run_ours(args, w):
                        "parallelism": "dp%d" % ws if ws > 1 else "single",
                        "l2": "inputs larger than L2 (W %.0f MiB > 129 MB); no flush" % (W.numel() * 2 / 2**20),
                        "chunk_budget_bytes": budget or (1 << 30),
-                       "filter_threshold": args.filter_threshold},
+                       "filter_threshold": args.filter_threshold, "sort_vocab": args.sort_vocab},
             # flops counted as the exact path's 8*N*Hd*V; a filtered run skips part of it
             "flops_basis": "8*N*Hd*V" + (" (exact work; filtering skips some)" if args.filter_threshold > 0 else ""),
             "pct_bf16_peak": 100.0 * flops / (ms * 1e-3) / (peaks["bf16"] * 1e12),
@@ -428,6 +435,8 @@ def main():
     ap.add_argument("--chunk-budget", type=int, default=0)
     ap.add_argument("--filter-threshold", type=float, default=0.0,
                     help="gradient filtering threshold (0 = exact backward; e.g. 2**-12 = 0.000244140625)")
+    ap.add_argument("--sort-vocab", action="store_true",
+                    help="backward walks the vocabulary in mean-logit order (pays with --filter-threshold)")
     ap.add_argument("--cpu-sample", type=int, default=1024)
     ap.add_argument("--ref-sample", type=int, default=64)
     ap.add_argument("--no-e2e", action="store_true")

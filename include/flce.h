@@ -73,6 +73,11 @@ typedef enum flce_reduction {
 
 /* counts[2] bits */
 #define FLCE_DEVERR_WAIT_TIMEOUT 1u  /* an mbarrier wait exceeded its limit */
+#define FLCE_DEVERR_BAD_INDEX 2u     /* a vocabulary order entry outside [0, V) (never
+                                        expected; the access it would index is skipped) */
+
+/* Backward options (bit flags). */
+#define FLCE_BWD_SORT_VOCAB 1u  /* process the vocabulary in sorted order (flce_vocab_order) */
 
 /* Bytes of scratch that flce_forward needs for these sizes (0 when N == 0 is fine).
    Returns 0 and sets no error for invalid sizes; flce_forward reports those. */
@@ -81,10 +86,15 @@ FLCE_API size_t flce_forward_workspace_size(int64_t N, int64_t Hd, int64_t V);
 /* Bytes of scratch that flce_backward needs.  The backward walks the vocabulary in
    chunks of Vc columns and keeps one bf16 [N, Vc] dZ chunk plus an fp32 [N, Hd] dH
    accumulator (the latter only when there is more than one chunk), plus one byte per
-   64 x 64 block of the chunk for the filtered mode.
-   chunk_budget_bytes bounds the dZ chunk (0 = default 1 GiB); the same value must be
-   passed to flce_backward. */
-FLCE_API size_t flce_backward_workspace_size(int64_t N, int64_t Hd, int64_t V, size_t chunk_budget_bytes);
+   64 x 64 block of the chunk for the filtered mode.  With FLCE_BWD_SORT_VOCAB it also
+   holds a bf16 [Vc, Hd] copy of the chunk's weight rows in sorted order and the order
+   itself (about 28 bytes per vocabulary row).
+   chunk_budget_bytes bounds the dZ chunk plus that weight copy (0 = default 1 GiB):
+   Vc = budget / (2 N), or budget / (2 N + 2 Hd) when sorting, rounded down to 256.
+   The same budget and options must be passed to flce_backward.  Unknown option bits:
+   returns 0. */
+FLCE_API size_t flce_backward_workspace_size(int64_t N, int64_t Hd, int64_t V, size_t chunk_budget_bytes,
+                                             unsigned options);
 
 /* Forward: loss, per-row LSE (saved for the backward), target logits and counts.
  *   H            (device) bf16 [N, Hd]
@@ -119,6 +129,12 @@ FLCE_API flce_status flce_forward(const void* H, const void* W, const int64_t* l
  *                every 64 x 64 (token x vocabulary) block of dZ left all zero is skipped
  *                by the dW and dH products.  An approximation; the exact path is the
  *                default.  Negative or NaN: FLCE_ERR_ARG.
+ *   options      0, or FLCE_BWD_SORT_VOCAB: walk the vocabulary in the order of
+ *                flce_vocab_order (mean logit descending) so that the entries that
+ *                survive filtering gather in few blocks and more blocks are skipped
+ *                (Liger-CCE blog, §三 "CCE", vocabulary sorting).  The gradients are the
+ *                same sums taken in another order; dW rows are written back to their
+ *                ids.  Other bits: FLCE_ERR_ARG.
  *   dH           (device) bf16 [N, Hd] (written)
  *   dW           (device) bf16 [V, Hd] (written, every row)
  *   workspace    (device) >= flce_backward_workspace_size(N, Hd, V, chunk_budget_bytes)
@@ -130,9 +146,25 @@ FLCE_API flce_status flce_backward(const void* H, const void* W, const int64_t* 
                           const float* lse, int64_t* counts,
                           int64_t N, int64_t Hd, int64_t V, int64_t ignore_index,
                           float softcap, int reduction, const float* grad_out,
-                          float filter_threshold, void* dH, void* dW,
+                          float filter_threshold, unsigned options, void* dH, void* dW,
                           void* workspace, size_t workspace_bytes, size_t chunk_budget_bytes,
                           void* stream);
+
+/* Vocabulary order used by FLCE_BWD_SORT_VOCAB (Liger-CCE blog, §三 "CCE": the mean
+ * logit of every word over the batch puts the frequent words next to each other).
+ *   keys  (device) fp32 [V] or NULL: key_v = (1/N) sum_i h_i . w_v, the raw logit
+ *         (before any softcap) averaged over all N rows, ignored rows included, computed
+ *         as hbar . w_v with hbar the fp32 column mean of H; 0 when N == 0
+ *   perm  (device) int32 [V]: perm[p] = the row placed at position p; keys descending,
+ *         equal keys (as fp32, -0 == +0) by ascending row
+ *   inv   (device) int32 [V] or NULL: inv[perm[p]] = p
+ *   workspace >= flce_vocab_order_workspace_size(N, Hd, V) bytes, 256-byte aligned.
+ * Deterministic (fixed summation and merge orders).  NaN keys sort in an unspecified
+ * place.  Errors as in flce_forward. */
+FLCE_API size_t flce_vocab_order_workspace_size(int64_t N, int64_t Hd, int64_t V);
+FLCE_API flce_status flce_vocab_order(const void* H, const void* W, int64_t N, int64_t Hd, int64_t V,
+                             float* keys, int32_t* perm, int32_t* inv,
+                             void* workspace, size_t workspace_bytes, void* stream);
 
 /* Forward pass that allocates nothing and takes no workspace.  The pages have no
  * counterpart: this entry point exists for callers that cannot allocate device memory
@@ -177,7 +209,8 @@ FLCE_API flce_status flce_forward_noalloc(const void* H, const void* W, const in
  *      complete) and dH_partial (fp32 [N, Hd], this shard's sum over its rows); the
  *      caller sums dH_partial over the shards (e.g. an all-reduce) and rounds as needed.
  *      A row whose label lives in another shard is still a valid row here.
- *      Workspace: flce_backward_workspace_size(N, Hd, V_shard, chunk_budget_bytes).
+ *      Workspace: flce_backward_workspace_size(N, Hd, V_shard, chunk_budget_bytes, options);
+ *      FLCE_BWD_SORT_VOCAB sorts this shard's rows only.
  * v_offset < 0, V_shard <= 0 or v_offset + V_shard > V_total: FLCE_ERR_ARG. */
 FLCE_API flce_status flce_forward_shard(const void* H, const void* W_shard, const int64_t* labels,
                                int64_t N, int64_t Hd, int64_t V_shard, int64_t v_offset,
@@ -197,7 +230,7 @@ FLCE_API flce_status flce_backward_shard(const void* H, const void* W_shard, con
                                 const float* lse, int64_t* counts, int64_t N, int64_t Hd,
                                 int64_t V_shard, int64_t v_offset, int64_t V_total,
                                 int64_t ignore_index, float softcap, int reduction,
-                                const float* grad_out, float filter_threshold,
+                                const float* grad_out, float filter_threshold, unsigned options,
                                 float* dH_partial, void* dW_shard, void* workspace,
                                 size_t workspace_bytes, size_t chunk_budget_bytes, void* stream);
 
@@ -235,6 +268,9 @@ FLCE_API int flce_last_cuda_error(void);
 #define FLCE_KERNEL_BLOCK_MASK 9  /* filtered backward: live K steps per dW / dH tile   */
 #define FLCE_KERNEL_SELFTEST 10   /* flce_selftest_wait_timeout                        */
 #define FLCE_KERNEL_SHARD_MERGE 11 /* vocabulary shards: fixed-order LSE / loss merge  */
+#define FLCE_KERNEL_VOCAB_KEYS 12  /* column mean of H, mean logit per vocabulary row     */
+#define FLCE_KERNEL_VOCAB_SORT 13  /* run sort + merge passes -> perm / inv               */
+#define FLCE_KERNEL_GATHER 14      /* sorted chunk's weight rows -> contiguous copy       */
 FLCE_API uint64_t flce_launch_count(void);
 FLCE_API int flce_set_event_sink(void* const* start_events, void* const* end_events, int* kernel_ids,
                         int capacity);

@@ -29,13 +29,15 @@ from . import _build
 __all__ = [
     "linear_cross_entropy", "FusedLinearCrossEntropyLoss", "flce_forward", "flce_backward", "flce_forward_shard", "flce_merge_shards",
     "flce_backward_shard", "forward_workspace_size",
-    "backward_workspace_size", "FlceError", "check_counts", "library", "launch_count",
+    "backward_workspace_size", "vocab_order", "FlceError", "check_counts", "library", "launch_count",
     "EventSink", "KERNEL_NAMES",
 ]
 
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 KERNEL_NAMES = {0: "label_dot", 1: "linear_lse", 2: "lse_merge", 3: "reduce", 4: "bwd_prep",
-                5: "dz", 6: "dw", 7: "dh", 8: "zero", 9: "block_mask", 10: "selftest", 11: "shard_merge"}
+                5: "dz", 6: "dw", 7: "dh", 8: "zero", 9: "block_mask", 10: "selftest", 11: "shard_merge",
+                12: "vocab_keys", 13: "vocab_sort", 14: "gather"}
+BWD_SORT_VOCAB = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -58,12 +60,17 @@ def library() -> ctypes.CDLL:
                                      ctypes.c_float, ctypes.c_int)
             lib.flce_forward_workspace_size.argtypes = [i64, i64, i64]
             lib.flce_forward_workspace_size.restype = sz
-            lib.flce_backward_workspace_size.argtypes = [i64, i64, i64, sz]
+            u32 = ctypes.c_uint
+            lib.flce_backward_workspace_size.argtypes = [i64, i64, i64, sz, u32]
             lib.flce_backward_workspace_size.restype = sz
             lib.flce_forward.argtypes = [vp, vp, vp, i64, i64, i64, i64, f32, i32, vp, vp, vp, vp, vp, sz, vp]
             lib.flce_forward.restype = i32
-            lib.flce_backward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, i32, vp, f32, vp, vp,
+            lib.flce_backward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, i32, vp, f32, u32, vp, vp,
                                           vp, sz, sz, vp]
+            lib.flce_vocab_order_workspace_size.argtypes = [i64, i64, i64]
+            lib.flce_vocab_order_workspace_size.restype = sz
+            lib.flce_vocab_order.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, vp, sz, vp]
+            lib.flce_vocab_order.restype = i32
             lib.flce_backward.restype = i32
             lib.flce_strerror.argtypes = [i32]
             lib.flce_strerror.restype = ctypes.c_char_p
@@ -79,7 +86,7 @@ def library() -> ctypes.CDLL:
             lib.flce_merge_shards.argtypes = [vp, vp, i64, vp, i64, i64, i64, i32, vp, vp, vp, vp, sz, vp]
             lib.flce_merge_shards.restype = i32
             lib.flce_backward_shard.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, i32, vp, f32,
-                                                vp, vp, vp, sz, sz, vp]
+                                                u32, vp, vp, vp, sz, sz, vp]
             lib.flce_backward_shard.restype = i32
             lib.flce_selftest_wait_timeout.argtypes = [vp, vp]
             lib.flce_selftest_wait_timeout.restype = i32
@@ -115,8 +122,30 @@ def forward_workspace_size(N: int, Hd: int, V: int) -> int:
     return int(library().flce_forward_workspace_size(N, Hd, V))
 
 
-def backward_workspace_size(N: int, Hd: int, V: int, chunk_budget: int = 0) -> int:
-    return int(library().flce_backward_workspace_size(N, Hd, V, chunk_budget))
+def backward_workspace_size(N: int, Hd: int, V: int, chunk_budget: int = 0, sort_vocab: bool = False) -> int:
+    return int(library().flce_backward_workspace_size(N, Hd, V, chunk_budget, BWD_SORT_VOCAB if sort_vocab else 0))
+
+
+def vocab_order(H, W, workspace=None):
+    """Sort keys (mean raw logit of every vocabulary row over the rows of H) and the
+    order the sorted backward walks: (keys fp32 [V], perm int32 [V], inv int32 [V]),
+    perm[p] = the row at position p, keys descending, ties by ascending row."""
+    if not (H.is_cuda and W.is_cuda and H.is_contiguous() and W.is_contiguous()):
+        raise FlceError("H and W must be contiguous CUDA tensors")
+    if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise FlceError("H and W must be bfloat16")
+    N, Hd = H.shape
+    V = W.shape[0]
+    dev = W.device
+    with torch.cuda.device(dev):
+        keys = torch.empty(V, dtype=torch.float32, device=dev)
+        perm = torch.empty(V, dtype=torch.int32, device=dev)
+        inv = torch.empty(V, dtype=torch.int32, device=dev)
+        need = int(library().flce_vocab_order_workspace_size(N, Hd, V))
+        ws = workspace if workspace is not None else torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        _check(library().flce_vocab_order(_p(H), _p(W), N, Hd, V, _p(keys), _p(perm), _p(inv), _p(ws), ws.numel(),
+                                          _stream(dev)))
+    return keys, perm, inv
 
 
 def _check_inputs(H, W, labels):
@@ -161,10 +190,12 @@ def flce_forward(H, W, labels, ignore_index: int = -100, softcap: float = 0.0, r
 
 def flce_backward(H, W, labels, lse, counts, grad_out, ignore_index: int = -100, softcap: float = 0.0,
                   reduction="mean", chunk_budget: int = 0, workspace=None, dH=None, dW=None,
-                  filter_threshold: float = 0.0):
+                  filter_threshold: float = 0.0, sort_vocab: bool = False):
     """One backward call from the saved LSE and counts.  Returns (dH, dW) in bf16.
     filter_threshold > 0 turns on gradient filtering (softmax entries below it, other
-    than the target, are dropped and all-zero blocks are skipped): an approximation."""
+    than the target, are dropped and all-zero blocks are skipped): an approximation.
+    sort_vocab walks the vocabulary in mean-logit order (see vocab_order), which gathers
+    the surviving entries into fewer blocks; the result is the same sums reordered."""
     _check_inputs(H, W, labels)
     red = _reduction(reduction)
     N, Hd = H.shape
@@ -176,11 +207,11 @@ def flce_backward(H, W, labels, lse, counts, grad_out, ignore_index: int = -100,
     with torch.cuda.device(dev):
         dH = dH if dH is not None else torch.empty_like(H)
         dW = dW if dW is not None else torch.empty_like(W)
-        need = backward_workspace_size(N, Hd, V, chunk_budget)
+        need = backward_workspace_size(N, Hd, V, chunk_budget, sort_vocab)
         ws = workspace if workspace is not None else torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         _check(library().flce_backward(_p(H), _p(W), _p(labels), _p(lse), _p(counts), N, Hd, V, int(ignore_index),
-                                       float(softcap), red, _p(g), float(filter_threshold), _p(dH), _p(dW), _p(ws),
-                                       ws.numel(),
+                                       float(softcap), red, _p(g), float(filter_threshold),
+                                       BWD_SORT_VOCAB if sort_vocab else 0, _p(dH), _p(dW), _p(ws), ws.numel(),
                                        int(chunk_budget), _stream(dev)))
     return dH, dW
 
@@ -228,7 +259,7 @@ def flce_merge_shards(lse_parts, target_parts, labels, V_total: int, ignore_inde
 
 def flce_backward_shard(H, W_shard, labels, lse, counts, grad_out, v_offset: int, V_total: int,
                         ignore_index: int = -100, softcap: float = 0.0, reduction="mean", chunk_budget: int = 0,
-                        filter_threshold: float = 0.0):
+                        filter_threshold: float = 0.0, sort_vocab: bool = False):
     """Backward over one vocabulary shard from the global lse and counts.  Returns
     (dH_partial fp32 [N, Hd], to be summed over the shards; dW_shard bf16)."""
     _check_inputs(H, W_shard, labels)
@@ -240,12 +271,12 @@ def flce_backward_shard(H, W_shard, labels, lse, counts, grad_out, v_offset: int
     with torch.cuda.device(dev):
         dh = torch.empty(N, Hd, dtype=torch.float32, device=dev)
         dw = torch.empty_like(W_shard)
-        need = backward_workspace_size(N, Hd, Vs, chunk_budget)
+        need = backward_workspace_size(N, Hd, Vs, chunk_budget, sort_vocab)
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         _check(library().flce_backward_shard(_p(H), _p(W_shard), _p(labels), _p(lse), _p(counts), N, Hd, Vs,
                                              int(v_offset), int(V_total), int(ignore_index), float(softcap), red,
-                                             _p(g), float(filter_threshold), _p(dh), _p(dw), _p(ws), ws.numel(),
-                                             int(chunk_budget), _stream(dev)))
+                                             _p(g), float(filter_threshold), BWD_SORT_VOCAB if sort_vocab else 0,
+                                             _p(dh), _p(dw), _p(ws), ws.numel(), int(chunk_budget), _stream(dev)))
     return dh, dw
 
 
@@ -254,7 +285,8 @@ def check_counts(counts) -> tuple[int, int]:
     device-side wait timeout; returns (n_valid, n_bad)."""
     c = counts.tolist()
     if c[2] != 0:
-        raise FlceError("device error bits %#x (a bounded wait expired)" % c[2])
+        raise FlceError("device error bits %#x (1: a bounded wait expired, 2: a vocabulary order index "
+                        "out of range)" % c[2])
     if c[1] != 0:
         raise FlceError("%d labels outside [0, V) that are not ignore_index" % c[1])
     return c[0], c[1]
@@ -262,33 +294,36 @@ def check_counts(counts) -> tuple[int, int]:
 
 class _FusedLinearCrossEntropy(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, H, W, labels, ignore_index, softcap, reduction, chunk_budget, filter_threshold):
+    def forward(ctx, H, W, labels, ignore_index, softcap, reduction, chunk_budget, filter_threshold, sort_vocab):
         loss, lse, counts, _ = flce_forward(H, W, labels, ignore_index, softcap, reduction)
         ctx.save_for_backward(H, W, labels, lse, counts)
-        ctx.cfg = (ignore_index, softcap, reduction, chunk_budget, filter_threshold)
+        ctx.cfg = (ignore_index, softcap, reduction, chunk_budget, filter_threshold, sort_vocab)
         return loss
 
     @staticmethod
     def backward(ctx, grad):
         H, W, labels, lse, counts = ctx.saved_tensors
-        ignore_index, softcap, reduction, chunk_budget, filter_threshold = ctx.cfg
+        ignore_index, softcap, reduction, chunk_budget, filter_threshold, sort_vocab = ctx.cfg
         dH, dW = flce_backward(H, W, labels, lse, counts, grad, ignore_index, softcap, reduction, chunk_budget,
-                               filter_threshold=filter_threshold)
+                               filter_threshold=filter_threshold, sort_vocab=sort_vocab)
         return (dH if ctx.needs_input_grad[0] else None, dW if ctx.needs_input_grad[1] else None,
-                None, None, None, None, None, None)
+                None, None, None, None, None, None, None)
 
 
 def linear_cross_entropy(hidden, weight, labels, ignore_index: int = -100, softcap: float = 0.0,
-                         reduction: str = "mean", chunk_budget: int = 0, filter_threshold: float = 0.0):
+                         reduction: str = "mean", chunk_budget: int = 0, filter_threshold: float = 0.0,
+                         sort_vocab: bool = False):
     """Cross-entropy of ``hidden @ weight.T`` against ``labels`` without materialising
     the logits.  ``hidden`` [..., Hd] bf16, ``weight`` [V, Hd] bf16, ``labels`` [...]
     int64.  reduction: "mean" (over rows whose label is valid), "sum" or "none".
-    filter_threshold > 0 (e.g. 2**-12) makes the backward approximate: see flce_backward."""
+    filter_threshold > 0 (e.g. 2**-12) makes the backward approximate, and sort_vocab
+    lets it skip more blocks: see flce_backward."""
     Hd = hidden.shape[-1]
     H2 = hidden.reshape(-1, Hd)
     y = labels.reshape(-1)
     out = _FusedLinearCrossEntropy.apply(H2.contiguous(), weight.contiguous(), y.contiguous(), int(ignore_index),
-                                         float(softcap), reduction, int(chunk_budget), float(filter_threshold))
+                                         float(softcap), reduction, int(chunk_budget), float(filter_threshold),
+                                         bool(sort_vocab))
     if reduction == "none":
         out = out.reshape(labels.shape)
     return out
@@ -305,7 +340,7 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
     """
 
     def __init__(self, ignore_index: int = -100, softcap: float = 0.0, reduction: str = "mean",
-                 chunk_budget: int = 0, filter_threshold: float = 0.0):
+                 chunk_budget: int = 0, filter_threshold: float = 0.0, sort_vocab: bool = False):
         super().__init__()
         _reduction(reduction)
         self.ignore_index = int(ignore_index)
@@ -313,14 +348,15 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
         self.reduction = reduction
         self.chunk_budget = int(chunk_budget)
         self.filter_threshold = float(filter_threshold)
+        self.sort_vocab = bool(sort_vocab)
 
     def forward(self, weight, hidden, labels):
         return linear_cross_entropy(hidden, weight, labels, self.ignore_index, self.softcap, self.reduction,
-                                    self.chunk_budget, self.filter_threshold)
+                                    self.chunk_budget, self.filter_threshold, self.sort_vocab)
 
     def extra_repr(self):
-        return "ignore_index=%d, softcap=%g, reduction=%s, filter_threshold=%g" % (
-            self.ignore_index, self.softcap, self.reduction, self.filter_threshold)
+        return "ignore_index=%d, softcap=%g, reduction=%s, filter_threshold=%g, sort_vocab=%s" % (
+            self.ignore_index, self.softcap, self.reduction, self.filter_threshold, self.sort_vocab)
 
 
 def launch_count() -> int:

@@ -11,6 +11,7 @@
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "small_kernels.cuh"
+#include "vocab_order.cuh"
 
 namespace flce {
 
@@ -215,20 +216,45 @@ flce_status plan_forward(int64_t N, int64_t Hd, int64_t V, int pairs, FwdPlan* p
   return FLCE_OK;
 }
 
+// Scratch of the vocabulary order, at offsets from `base` inside a larger workspace.
+struct VocabPlan {
+  int n_seg = 0;
+  int64_t rows_per_seg = 0;
+  size_t off_key = 0, off_word0 = 0, off_word1 = 0, off_perm = 0, off_inv = 0, off_part = 0, off_hbar = 0;
+};
+
+bool plan_vocab(int64_t N, int64_t Hd, int64_t V, size_t* cur, VocabPlan* p) {
+  p->n_seg = static_cast<int>(std::min<int64_t>(128, std::max<int64_t>(1, cdiv(N, 64))));
+  p->rows_per_seg = std::max<int64_t>(1, cdiv(N, p->n_seg));
+  size_t part;
+  if (!mul_ok(size_t(p->n_seg), size_t(Hd), &part) || !mul_ok(part, 4, &part)) return false;
+  return reserve(cur, size_t(V) * 4, &p->off_key) && reserve(cur, size_t(V) * 8, &p->off_word0) &&
+         reserve(cur, size_t(V) * 8, &p->off_word1) && reserve(cur, size_t(V) * 4, &p->off_perm) &&
+         reserve(cur, size_t(V) * 4, &p->off_inv) && reserve(cur, part, &p->off_part) &&
+         reserve(cur, size_t(Hd) * 4, &p->off_hbar);
+}
+
 struct BwdPlan {
   int64_t Vc = 0;
   int n_chunks = 0;
   int nz_rows = 0, nz_ld = 0;  // token blocks x vocabulary blocks of the dZ block flags
   int dh_mask_ld = 0, dw_mask_ld = 0, mask_tok_tiles = 0, mask_voc_tiles = 0;
-  size_t off_rows = 0, off_dz = 0, off_dh = 0, off_nz = 0, off_dh_mask = 0, off_dw_mask = 0, total = 0;
+  bool sort = false;
+  VocabPlan vocab;
+  size_t off_rows = 0, off_dz = 0, off_dh = 0, off_nz = 0, off_dh_mask = 0, off_dw_mask = 0, off_wperm = 0, total = 0;
 };
 
-flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, BwdPlan* p) {
+// The chunk budget covers the bf16 dZ chunk and, with the sorted vocabulary, the bf16
+// copy of the chunk's weight rows in sorted order: Vc = budget / (2N (+ 2Hd)).
+flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, unsigned options, BwdPlan* p) {
   flce_status s = check_sizes(N, Hd, V);
   if (s != FLCE_OK) return s;
+  if ((options & ~unsigned(FLCE_BWD_SORT_VOCAB)) != 0) return FLCE_ERR_ARG;
+  p->sort = (options & FLCE_BWD_SORT_VOCAB) != 0;
   if (budget == 0) budget = kDefaultChunkBudget;
   const int64_t v_round = int64_t(cdiv(V, kBN)) * kBN;
-  int64_t vc = N > 0 ? static_cast<int64_t>(budget / (size_t(N) * 2)) : v_round;
+  const size_t per_col = size_t(N) * 2 + (p->sort ? size_t(Hd) * 2 : 0);
+  int64_t vc = N > 0 ? static_cast<int64_t>(budget / per_col) : v_round;
   vc = vc / kBN * kBN;
   if (vc < kBN) vc = kBN;
   if (vc > v_round) vc = v_round;
@@ -248,6 +274,12 @@ flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, BwdPl
       !reserve(&cur, size_t(p->mask_tok_tiles) * p->dh_mask_ld * 4, &p->off_dh_mask) ||
       !reserve(&cur, size_t(p->mask_voc_tiles) * p->dw_mask_ld * 4, &p->off_dw_mask))
     return FLCE_ERR_OVERFLOW;
+  if (p->sort) {
+    size_t wp;
+    if (!mul_ok(size_t(vc), size_t(Hd), &wp) || !mul_ok(wp, 2, &wp) || !reserve(&cur, wp, &p->off_wperm) ||
+        !plan_vocab(N, Hd, V, &cur, &p->vocab))
+      return FLCE_ERR_OVERFLOW;
+  }
   p->total = align_up(cur);
   return FLCE_OK;
 }
@@ -255,6 +287,62 @@ flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, BwdPl
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
+
+// Sort keys (mean raw logit per vocabulary row), then the stable descending order:
+// perm[position] = row, inv[row] = position (inv may be null).
+flce_status vocab_order_impl(const void* H, const void* W, int64_t N, int64_t Hd, int64_t V, const VocabPlan& vp,
+                             uint8_t* ws, float* key, int32_t* perm, int32_t* inv, unsigned long long* err, int sms,
+                             cudaStream_t st) {
+  const __nv_bfloat16* Hb = static_cast<const __nv_bfloat16*>(H);
+  const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
+  unsigned long long* w0 = reinterpret_cast<unsigned long long*>(ws + vp.off_word0);
+  unsigned long long* w1 = reinterpret_cast<unsigned long long*>(ws + vp.off_word1);
+  float* part = reinterpret_cast<float*>(ws + vp.off_part);
+  float* hbar = reinterpret_cast<float*>(ws + vp.off_hbar);
+  cudaError_t e;
+  if (N == 0) {  // no rows: every key is 0 (hbar = 0), the order is the identity
+    if ((e = cudaMemsetAsync(hbar, 0, size_t(Hd) * 4, st)) != cudaSuccess) return cuda_fail(e);
+  } else {
+    e = launch(FLCE_KERNEL_VOCAB_KEYS, st, [&] {
+      k_col_partial<<<dim3(cdiv(Hd, 8 * kColThreads), vp.n_seg), kColThreads, 0, st>>>(Hb, N, Hd, vp.rows_per_seg,
+                                                                                        part);
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch(FLCE_KERNEL_VOCAB_KEYS, st, [&] {
+      k_col_mean<<<cdiv(Hd, 256), 256, 0, st>>>(part, vp.n_seg, Hd, N, hbar);
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  const int row_blocks = std::min(cdiv(V, kRowCopyThreads / 32), 8 * sms);
+  e = launch(FLCE_KERNEL_VOCAB_KEYS, st, [&] {
+    k_vocab_keys<<<row_blocks, kRowCopyThreads, 0, st>>>(Wb, hbar, V, Hd, key, w0);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch(FLCE_KERNEL_VOCAB_SORT, st, [&] {
+    k_sort_runs<<<cdiv(V, kSortSeg), kSortThreads, 0, st>>>(w0, w1, V);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned long long* cur = w1;
+  unsigned long long* nxt = w0;
+  const int merge_blocks = std::min(cdiv(V, kMergeSortThreads), 8 * sms);
+  for (int64_t L = kSortSeg; L < V; L *= 2) {
+    e = launch(FLCE_KERNEL_VOCAB_SORT, st, [&] {
+      k_merge_runs<<<merge_blocks, kMergeSortThreads, 0, st>>>(cur, nxt, V, L);
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return cuda_fail(e);
+    std::swap(cur, nxt);
+  }
+  e = launch(FLCE_KERNEL_VOCAB_SORT, st, [&] {
+    k_order_finish<<<merge_blocks, kMergeSortThreads, 0, st>>>(cur, V, perm, inv, err);
+    return cudaGetLastError();
+  });
+  return e == cudaSuccess ? FLCE_OK : cuda_fail(e);
+}
 
 // Forward over the weight rows [v_offset, v_offset + V) of a vocabulary of V_total
 // (v_offset = 0 and V_total = V without sharding).  reduction -1: no loss output (the
@@ -343,13 +431,13 @@ flce_status forward_impl(const void* H, const void* W, const int64_t* labels, in
 // shard's partial sum over its vocabulary rows instead of as bf16 into dH.
 flce_status backward_impl(const void* H, const void* W, const int64_t* labels, const float* lse, int64_t* counts,
                           int64_t N, int64_t Hd, int64_t V, int64_t v_offset, int64_t V_total, int64_t ignore_index,
-                          float softcap, int reduction, const float* grad_out, float filter_threshold, void* dH,
-                          float* dh_partial, void* dW, void* workspace, size_t workspace_bytes,
-                          size_t chunk_budget_bytes, void* stream) {
+                          float softcap, int reduction, const float* grad_out, float filter_threshold,
+                          unsigned options, void* dH, float* dh_partial, void* dW, void* workspace,
+                          size_t workspace_bytes, size_t chunk_budget_bytes, void* stream) {
   if (reduction < 0 || reduction > 2 || softcap != softcap || !(filter_threshold >= 0.0f)) return FLCE_ERR_ARG;
   const bool filter = filter_threshold > 0.0f;
   BwdPlan pl;
-  flce_status s = plan_backward(N, Hd, V, chunk_budget_bytes, &pl);
+  flce_status s = plan_backward(N, Hd, V, chunk_budget_bytes, options, &pl);
   if (s != FLCE_OK) return s;
   if (!W || !dW || !counts) return FLCE_ERR_ARG;
   if (N > 0 && (!H || !labels || !lse || !grad_out || (!dH && !dh_partial) || !workspace)) return FLCE_ERR_ARG;
@@ -379,16 +467,30 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
   const bool skip = filter && pl.dh_mask_ld <= kMaskWords && pl.dw_mask_ld <= kMaskWords;
   unsigned long long* err = reinterpret_cast<unsigned long long*>(counts + 2);
 
+  // Sorted vocabulary: chunk c covers positions [c Vc, (c + 1) Vc) of the order; its
+  // weight rows are gathered into wperm, labels become positions, dW rows go back to ids.
+  int32_t* perm = nullptr;
+  int32_t* inv = nullptr;
+  __nv_bfloat16* wperm = nullptr;
+  if (pl.sort) {
+    perm = reinterpret_cast<int32_t*>(ws + pl.vocab.off_perm);
+    inv = reinterpret_cast<int32_t*>(ws + pl.vocab.off_inv);
+    wperm = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_wperm);
+    s = vocab_order_impl(H, W, N, Hd, V, pl.vocab, ws, reinterpret_cast<float*>(ws + pl.vocab.off_key), perm, inv,
+                         err, sms, st);
+    if (s != FLCE_OK) return s;
+  }
+
   e = launch(FLCE_KERNEL_BWD_PREP, st, [&] {
     k_bwd_prep<<<cdiv(N, 256), 256, 0, st>>>(labels, lse, counts, grad_out, reduction, N, V, v_offset, V_total,
-                                             ignore_index, rows);
+                                             ignore_index, inv, rows);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e);
 
   CUtensorMap tmH_k, tmW_k, tmH_mn, tmW_mn;
-  if (!tmap_2d(&tmH_k, H, Hd, N, Hd * 2, kBK, kBM) || !tmap_2d(&tmW_k, W, Hd, V, Hd * 2, kBK, kBN / 2) ||
-      !tmap_2d(&tmH_mn, H, Hd, N, Hd * 2, 64, kBK) || !tmap_2d(&tmW_mn, W, Hd, V, Hd * 2, 64, kBK))
+  if (!tmap_2d(&tmH_k, H, Hd, N, Hd * 2, kBK, kBM) || !tmap_2d(&tmH_mn, H, Hd, N, Hd * 2, 64, kBK) ||
+      (!pl.sort && (!tmap_2d(&tmW_k, W, Hd, V, Hd * 2, kBK, kBN / 2) || !tmap_2d(&tmW_mn, W, Hd, V, Hd * 2, 64, kBK))))
     return FLCE_ERR_CUDA;
 
   const int m_tiles_tok = cdiv(N, kPairM);
@@ -399,6 +501,18 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
     CUtensorMap tmDz_k, tmDz_mn;
     if (!tmap_2d(&tmDz_k, dz, wc, N, pl.Vc * 2, kBK, kBM) || !tmap_2d(&tmDz_mn, dz, wc, N, pl.Vc * 2, 64, kBK))
       return FLCE_ERR_CUDA;
+    int64_t w_off = v0;  // first weight row of the chunk in the tensor maps
+    if (pl.sort) {
+      e = launch(FLCE_KERNEL_GATHER, st, [&] {
+        k_gather_rows<<<std::min(cdiv(wc, kRowCopyThreads / 32), 8 * sms), kRowCopyThreads, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(W), V, Hd, perm, v0, wc, wperm, err);
+        return cudaGetLastError();
+      });
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (!tmap_2d(&tmW_k, wperm, Hd, wc, Hd * 2, kBK, kBN / 2) || !tmap_2d(&tmW_mn, wperm, Hd, wc, Hd * 2, 64, kBK))
+        return FLCE_ERR_CUDA;
+      w_off = 0;
+    }
 
     // dZ chunk = f(H W_chunk^T)
     Sched s4{};
@@ -409,7 +523,7 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
     s4.n_groups = s4.n_tiles;
     s4.units = s4.m_tiles * s4.n_groups;
     s4.order = 0;
-    s4.b_n_off = static_cast<int>(v0);
+    s4.b_n_off = static_cast<int>(w_off);
     if (filter && (e = cudaMemsetAsync(nz, 0, size_t(pl.nz_rows) * size_t(pl.nz_ld), st)) != cudaSuccess)
       return cuda_fail(e);
     EpiDzParams p4{N, V, v0, wc, pl.Vc, softcap, rows, dz, filter_threshold, nz, pl.nz_ld};
@@ -442,7 +556,7 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
       s5.kmask = dw_mask;
       s5.kmask_ld = pl.dw_mask_ld;
     }
-    EpiDwParams p5{wc, v0, Hd, static_cast<__nv_bfloat16*>(dW)};
+    EpiDwParams p5{wc, v0, Hd, static_cast<__nv_bfloat16*>(dW), perm, V};
     e = launch(FLCE_KERNEL_DW, st,
                [&] { return launch_dw(tmDz_mn, tmH_mn, s5, p5, err, pair_grid(s5.units, sms), st); });
     if (e != cudaSuccess) return cuda_fail(e);
@@ -456,7 +570,7 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
     s6.n_groups = d_tiles;
     s6.units = s6.m_tiles * s6.n_groups;
     s6.order = 1;
-    s6.b_k_off = static_cast<int>(v0);
+    s6.b_k_off = static_cast<int>(w_off);
     if (skip) {
       s6.kmask = dh_mask;
       s6.kmask_ld = pl.dh_mask_ld;
@@ -482,9 +596,35 @@ size_t flce_forward_workspace_size(int64_t N, int64_t Hd, int64_t V) {
   return plan_forward(N, Hd, V, kPlanPairs, &p) == FLCE_OK ? p.total : 0;
 }
 
-size_t flce_backward_workspace_size(int64_t N, int64_t Hd, int64_t V, size_t chunk_budget_bytes) {
+size_t flce_backward_workspace_size(int64_t N, int64_t Hd, int64_t V, size_t chunk_budget_bytes, unsigned options) {
   BwdPlan p;
-  return plan_backward(N, Hd, V, chunk_budget_bytes, &p) == FLCE_OK ? p.total : 0;
+  return plan_backward(N, Hd, V, chunk_budget_bytes, options, &p) == FLCE_OK ? p.total : 0;
+}
+
+size_t flce_vocab_order_workspace_size(int64_t N, int64_t Hd, int64_t V) {
+  VocabPlan p;
+  size_t cur = 0;
+  if (check_sizes(N, Hd, V) != FLCE_OK || !plan_vocab(N, Hd, V, &cur, &p)) return 0;
+  return align_up(cur);
+}
+
+flce_status flce_vocab_order(const void* H, const void* W, int64_t N, int64_t Hd, int64_t V, float* keys,
+                             int32_t* perm, int32_t* inv, void* workspace, size_t workspace_bytes, void* stream) {
+  flce_status s = check_sizes(N, Hd, V);
+  if (s != FLCE_OK) return s;
+  VocabPlan vp;
+  size_t cur = 0;
+  if (!plan_vocab(N, Hd, V, &cur, &vp)) return FLCE_ERR_OVERFLOW;
+  if (!W || !perm || !workspace || (N > 0 && !H)) return FLCE_ERR_ARG;
+  if (!aligned(W, 16) || (H && !aligned(H, 16)) || !aligned(perm, 4) || (keys && !aligned(keys, 4)) ||
+      (inv && !aligned(inv, 4)))
+    return FLCE_ERR_ALIGN;
+  if (workspace_bytes < align_up(cur) || !aligned(workspace, kAlign)) return FLCE_ERR_WORKSPACE;
+  int sms = 0;
+  if ((s = device_setup(&sms)) != FLCE_OK) return s;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return vocab_order_impl(H, W, N, Hd, V, vp, ws, keys ? keys : reinterpret_cast<float*>(ws + vp.off_key), perm, inv,
+                          nullptr, sms, static_cast<cudaStream_t>(stream));
 }
 
 flce_status flce_forward(const void* H, const void* W, const int64_t* labels, int64_t N, int64_t Hd, int64_t V,
@@ -498,11 +638,12 @@ flce_status flce_forward(const void* H, const void* W, const int64_t* labels, in
 
 flce_status flce_backward(const void* H, const void* W, const int64_t* labels, const float* lse, int64_t* counts,
                           int64_t N, int64_t Hd, int64_t V, int64_t ignore_index, float softcap, int reduction,
-                          const float* grad_out, float filter_threshold, void* dH, void* dW, void* workspace,
-                          size_t workspace_bytes, size_t chunk_budget_bytes, void* stream) {
+                          const float* grad_out, float filter_threshold, unsigned options, void* dH, void* dW,
+                          void* workspace, size_t workspace_bytes, size_t chunk_budget_bytes, void* stream) {
   if (N > 0 && !dH) return FLCE_ERR_ARG;
   return backward_impl(H, W, labels, lse, counts, N, Hd, V, 0, V, ignore_index, softcap, reduction, grad_out,
-                       filter_threshold, dH, nullptr, dW, workspace, workspace_bytes, chunk_budget_bytes, stream);
+                       filter_threshold, options, dH, nullptr, dW, workspace, workspace_bytes, chunk_budget_bytes,
+                       stream);
 }
 
 namespace {
@@ -576,13 +717,14 @@ flce_status flce_merge_shards(const float* lse_parts, const float* target_parts,
 flce_status flce_backward_shard(const void* H, const void* W_shard, const int64_t* labels, const float* lse,
                                 int64_t* counts, int64_t N, int64_t Hd, int64_t V_shard, int64_t v_offset,
                                 int64_t V_total, int64_t ignore_index, float softcap, int reduction,
-                                const float* grad_out, float filter_threshold, float* dH_partial, void* dW_shard,
-                                void* workspace, size_t workspace_bytes, size_t chunk_budget_bytes, void* stream) {
+                                const float* grad_out, float filter_threshold, unsigned options,
+                                float* dH_partial, void* dW_shard, void* workspace, size_t workspace_bytes,
+                                size_t chunk_budget_bytes, void* stream) {
   flce_status s = check_shard(V_shard, v_offset, V_total);
   if (s != FLCE_OK) return s;
   if (N > 0 && !dH_partial) return FLCE_ERR_ARG;
   return backward_impl(H, W_shard, labels, lse, counts, N, Hd, V_shard, v_offset, V_total, ignore_index, softcap,
-                       reduction, grad_out, filter_threshold, nullptr, dH_partial, dW_shard, workspace,
+                       reduction, grad_out, filter_threshold, options, nullptr, dH_partial, dW_shard, workspace,
                        workspace_bytes, chunk_budget_bytes, stream);
 }
 

@@ -82,10 +82,12 @@ struct EpiDzParams {
 };
 
 struct EpiDwParams {
-  int64_t rows_valid;   // chunk width: dZ^T rows that exist
-  int64_t row0;         // first output row (vocabulary index)
-  int64_t cols;         // Hd
-  __nv_bfloat16* out;   // dW, row pitch Hd
+  int64_t rows_valid;    // chunk width: dZ^T rows that exist
+  int64_t row0;          // first output row (vocabulary index, or position when sorted)
+  int64_t cols;          // Hd
+  __nv_bfloat16* out;    // dW, row pitch Hd
+  const int32_t* perm;   // sorted vocabulary: output row of position q is perm[q]; else null
+  int64_t out_rows;      // rows of dW (bound for the perm indirection)
 };
 
 struct EpiDhParams {

@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(256)
 __global__ void k_bwd_prep(const int64_t* __restrict__ labels, const float* __restrict__ lse,
                            const int64_t* __restrict__ counts, const float* __restrict__ grad,
                            int reduction, int64_t N, int64_t V, int64_t v_offset, int64_t V_total, int64_t ignore,
-                           RowInfo* __restrict__ out) {
+                           const int32_t* __restrict__ inv, RowInfo* __restrict__ out) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= N) return;
   const int64_t y = labels[i];
@@ -178,7 +178,8 @@ __global__ void k_bwd_prep(const int64_t* __restrict__ labels, const float* __re
   RowInfo r;
   r.lse2 = lse[i] * kLog2e;
   r.scale = scale;
-  r.label = (valid && yl >= 0 && yl < V) ? static_cast<int32_t>(yl) : -1;
+  // the target's column: its id in this vocabulary, or its position when sorted (inv)
+  r.label = (valid && yl >= 0 && yl < V) ? (inv ? inv[yl] : static_cast<int32_t>(yl)) : -1;
   r.pad = 0;
   out[i] = r;
 }

@@ -220,8 +220,13 @@ struct EpiDw {
   __device__ static void unit_begin(const Params&, State&) {}
   __device__ static void unit_end(const Params&, State&, int64_t, int, int) {}
   __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h) {
-    const bool row_ok = row < p.rows_valid;
-    __nv_bfloat16* out_row = p.out + (p.row0 + (row_ok ? row : 0)) * p.cols;
+    bool row_ok = row < p.rows_valid;
+    int64_t orow = p.row0 + (row_ok ? row : 0);
+    if (p.perm != nullptr && row_ok) {  // sorted vocabulary: position -> id
+      orow = p.perm[orow];
+      row_ok = orow >= 0 && orow < p.out_rows;
+    }
+    __nv_bfloat16* out_row = p.out + (row_ok ? orow : 0) * p.cols;
     for_each_slice(taddr, h, [&](int c, float(&x)[32]) {
       const int64_t col = static_cast<int64_t>(nt) * kBN + c * 32;
       if (!row_ok || col >= p.cols) return;

@@ -64,12 +64,24 @@ def test_workspace_sizes(lib):
     # one byte per 64 x 64 block of the chunk for the filtered mode
     budget = 64 << 20
     vc = (budget // (2 * n)) // 256 * 256
-    size = b(n, hd, v, budget)
+    size = b(n, hd, v, budget, 0)
     flags = (n // 64) * (vc // 64)
     assert size >= n * vc * 2 + n * hd * 4 + n * 16 + flags
     assert size < n * vc * 2 + n * hd * 4 + n * 16 + flags + (1 << 12)
     # a single chunk needs no fp32 accumulator
-    assert b(256, 64, 2000, 0) < 256 * 2048 * 2 + 256 * 16 + 4096
+    assert b(256, 64, 2000, 0, 0) < 256 * 2048 * 2 + 256 * 16 + 4096
+    # the sorted vocabulary: the budget also covers the sorted bf16 weight rows of the
+    # chunk, Vc = budget / (2N + 2Hd), plus the order (key, two sort words, perm, inv:
+    # 28 bytes per vocabulary row) and the column sums of H
+    vs = (budget // (2 * n + 2 * hd)) // 256 * 256
+    flags_s = (n // 64) * (vs // 64)
+    size_s = b(n, hd, v, budget, 1)
+    base = n * vs * 2 + vs * hd * 2 + n * hd * 4 + n * 16 + flags_s + 28 * v + 128 * hd * 4 + hd * 4
+    assert base <= size_s < base + (1 << 13)
+    assert b(n, hd, v, budget, 2) == 0 and b(n, hd, v, budget, 0x80000000) == 0
+    o = lib.flce_vocab_order_workspace_size
+    assert 28 * v + 128 * hd * 4 + hd * 4 <= o(n, hd, v) < 28 * v + 128 * hd * 4 + hd * 4 + (1 << 12)
+    assert o(0, 64, 10) > 0 and o(8, 60, 10) == 0 and o(8, 64, 0) == 0
 
 
 def _fwd(lib, H=0x1000, W=0x2000, labels=0x3000, N=16, Hd=64, V=100, red=0, loss=0x4000, lse=0x5000,
@@ -77,9 +89,9 @@ def _fwd(lib, H=0x1000, W=0x2000, labels=0x3000, N=16, Hd=64, V=100, red=0, loss
     return lib.flce_forward(H, W, labels, N, Hd, V, -100, softcap, red, loss, lse, None, counts, ws, ws_bytes, None)
 
 
-def _bwd(lib, N=16, Hd=64, V=100, red=0, filt=0.0, ws_bytes=1 << 24, dW=0x7000, W=0x2000):
-    return lib.flce_backward(0x1000, W, 0x3000, 0x5000, 0x6000, N, Hd, V, -100, 0.0, red, 0x8000, filt, 0x9000,
-                             dW, 0x10000, ws_bytes, 0, None)
+def _bwd(lib, N=16, Hd=64, V=100, red=0, filt=0.0, ws_bytes=1 << 24, dW=0x7000, W=0x2000, options=0):
+    return lib.flce_backward(0x1000, W, 0x3000, 0x5000, 0x6000, N, Hd, V, -100, 0.0, red, 0x8000, filt, options,
+                             0x9000, dW, 0x10000, ws_bytes, 0, None)
 
 
 def test_argument_errors_before_any_device_work(lib):
@@ -100,6 +112,13 @@ def test_argument_errors_before_any_device_work(lib):
     assert _bwd(lib, dW=None) == ARG
     assert _bwd(lib, ws_bytes=16) == WS
     assert _bwd(lib, W=0x2002) == ALIGN
+    assert _bwd(lib, options=2) == ARG
+    assert _bwd(lib, options=1, ws_bytes=lib.flce_backward_workspace_size(16, 64, 100, 0, 0)) == WS
+    vo = lambda H=0x1000, W=0x2000, perm=0x3000, ws_bytes=1 << 20, Hd=64: lib.flce_vocab_order(
+        H, W, 16, Hd, 100, None, perm, None, 0x10000, ws_bytes, None)
+    assert vo(perm=None) == ARG and vo(W=None) == ARG and vo(H=None) == ARG
+    assert vo(W=0x2008) == ALIGN and vo(perm=0x3002) == ALIGN and vo(Hd=60) == ALIGN
+    assert vo(ws_bytes=16) == WS
 
 
 def test_shard_argument_errors(lib):
@@ -110,7 +129,7 @@ def test_shard_argument_errors(lib):
     assert f(0, 0, 300) == ARG
     assert f(100, 0, 1 << 40) == OVERFLOW
     b = lambda off, vt: lib.flce_backward_shard(0x1000, 0x2000, 0x3000, 0x5000, 0x6000, 16, 64, 100, off, vt, -100,
-                                                0.0, 0, 0x8000, 0.0, 0x9000, 0x7000, 0x10000, 1 << 24, 0, None)
+                                                0.0, 0, 0x8000, 0.0, 0, 0x9000, 0x7000, 0x10000, 1 << 24, 0, None)
     assert b(-5, 300) == ARG and b(201, 300) == ARG
     m = lambda n, red: lib.flce_merge_shards(0x1000, 0x2000, n, 0x3000, 16, 300, -100, red, 0x4000, 0x5000, 0x6000,
                                              0x10000, 1 << 20, None)
