@@ -298,10 +298,30 @@ __device__ __forceinline__ void load_kmask(const Sched& s, int mt, uint32_t* mas
   for (int w = 0; w < words; ++w) mask[w] = __ldg(src + w);
 }
 
-// A K step is run when active, and the last one is run anyway when none was, so that
-// the accumulator of an all-zero tile is initialised (to zero).
-__device__ __forceinline__ bool kblock_run(const Sched& s, const uint32_t* mask, int kb, int done) {
-  return ((mask[kb >> 5] >> (kb & 31)) & 1u) != 0 || (kb == s.k_blocks - 1 && done == 0);
+// Calls f(kb), in increasing order, for every K step the tile runs: the steps whose
+// mask bit is set, or the last step alone when no bit is set (so that the accumulator
+// of an all-zero tile is initialised, to zero).  The mask is read one 32-step word at
+// a time and only set bits are visited, so a skipped step costs nothing.  Returns false
+// as soon as f does.
+template <class F>
+__device__ __forceinline__ bool for_each_live_kblock(const Sched& s, const uint32_t* mask, F&& f) {
+  const int words = (s.k_blocks + 31) / 32;
+  const uint32_t tail = (s.k_blocks & 31) ? ((1u << (s.k_blocks & 31)) - 1u) : 0xffffffffu;
+  bool any = false;
+  for (int wd = 0; wd < words; ++wd) {
+    uint32_t bits = mask[wd];
+    if (wd == words - 1) {
+      bits &= tail;
+      if (!any && bits == 0) bits = 1u << ((s.k_blocks - 1) & 31);
+    }
+    while (bits != 0) {
+      const int j = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      any = true;
+      if (!f(wd * 32 + j)) return false;
+    }
+  }
+  return true;
 }
 
 template <bool MN>
@@ -406,15 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {  // filtered dZ: only the K steps of the tile's mask
             uint32_t* mask = kmask;
             load_kmask(sched, mt, mask);
-            int done = 0;
-            for (int kb = 0; kb < sched.k_blocks; ++kb) {
-              if (!kblock_run(sched, mask, kb, done)) continue;
-              ++done;
-              if (!load_step(kb)) {
-                ok = false;
-                break;
-              }
-            }
+            if (!for_each_live_kblock(sched, mask, load_step)) ok = false;
           }
         }
       }
@@ -469,12 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t* mask = kmask + kMaskWords;
             load_kmask(sched, mt, mask);
             int done = 0;
-            for (int kb = 0; kb < sched.k_blocks; ++kb) {
-              if (!kblock_run(sched, mask, kb, done)) continue;
-              if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, err)) {
-                ok = false;
-                break;
-              }
+            ok = for_each_live_kblock(sched, mask, [&](int) -> bool {
+              if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, err)) return false;
               tc_fence_after();
               const uint32_t a = tiles_u32 + stage * kPairStageBytes;
               const uint32_t b = a + kATileBytes;
@@ -489,7 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 stage = 0;
                 phase ^= 1;
               }
-            }
+              return true;
+            });
           }
           if (!ok) break;
           mma_commit_pair(tfull0 + 8 * acc, 0x3);
