@@ -27,8 +27,9 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;              // TMA warp, MMA warp
 constexpr int kTmemCols = 2 * kBN;                         // double-buffered accumulator
 constexpr int kBarrierBytes = 256;
 constexpr int kMaskWords = 512;                            // K-step bitmask words (16384 steps)
-constexpr size_t kPairSmemBytes =
-    1024 + size_t(kPairStages) * kPairStageBytes + kBarrierBytes + 2 * kMaskWords * sizeof(uint32_t);
+constexpr int kEpiStageBytes = 4096;                       // per epilogue warp: 32 rows x 128 B
+constexpr size_t kPairSmemBytes = 1024 + size_t(kPairStages) * kPairStageBytes + kBarrierBytes +
+                                  2 * kMaskWords * sizeof(uint32_t) + size_t(kEpiWarps) * kEpiStageBytes;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;

@@ -112,7 +112,7 @@ struct EpiLse {
       st.m = mn;
     });
   }
-  __device__ static void tile(const Params& p, State& st, uint32_t taddr, int64_t, int nt, int h) {
+  __device__ static void tile(const Params& p, State& st, uint32_t taddr, int64_t, int nt, int h, uint8_t*) {
     if (p.softcap > 0.0f)
       slices<true>(p, st, taddr, nt, h);
     else
@@ -197,7 +197,7 @@ struct EpiDz {
       }
     });
   }
-  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h) {
+  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h, uint8_t*) {
     const bool cap = p.softcap > 0.0f;
     if (p.nz != nullptr) {
       if (cap)
@@ -214,72 +214,114 @@ struct EpiDz {
 };
 
 // Backward: dW chunk = dZ^T H, converted to bf16 and written once.
+// The dW and dH epilogues write through a per-warp staging buffer: each thread drops its
+// row's slice (32 columns) into shared memory, then the warp writes rows back as whole
+// 64- or 128-byte segments (8 or 4 rows per store instruction) instead of one 16-byte
+// piece of 32 different rows.  The 16-byte chunks of a staged row are XOR-swizzled by the
+// row index so that both the row-wise writes and the chunk-wise reads are free of bank
+// conflicts.
+
+// Backward: dW rows of the chunk = dZ_chunk^T H, bf16.
 struct EpiDw {
   using Params = EpiDwParams;
   struct State {};
   __device__ static void unit_begin(const Params&, State&) {}
   __device__ static void unit_end(const Params&, State&, int64_t, int, int) {}
-  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h) {
+  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h, uint8_t* stage) {
+    const int lane = threadIdx.x & 31;
     bool row_ok = row < p.rows_valid;
     int64_t orow = p.row0 + (row_ok ? row : 0);
     if (p.perm != nullptr && row_ok) {  // sorted vocabulary: position -> id
       orow = p.perm[orow];
       row_ok = orow >= 0 && orow < p.out_rows;
     }
-    __nv_bfloat16* out_row = p.out + (row_ok ? orow : 0) * p.cols;
+    const int64_t mine = row_ok ? orow : -1;
+    // store step i writes rows 8i .. 8i+7 of the warp: lane -> row 8i + lane/4, chunk lane%4
+    int64_t dst[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = __shfl_sync(0xffffffffu, mine, 8 * i + (lane >> 2));
+    const int ch = lane & 3;
     for_each_slice(taddr, h, [&](int c, float(&x)[32]) {
       const int64_t col = static_cast<int64_t>(nt) * kBN + c * 32;
-      if (!row_ok || col >= p.cols) return;
+      if (col >= p.cols) return;  // same for the whole warp
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (col + 8 * k + 8 <= p.cols) {
-          uint4 v = make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
-                               pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
-          *reinterpret_cast<uint4*>(out_row + col + 8 * k) = v;
-        }
+      for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<uint4*>(stage + lane * 64 + 16 * (k ^ ((lane >> 1) & 3))) =
+            make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
+                       pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rr = 8 * i + (lane >> 2);
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 64 + 16 * (ch ^ ((rr >> 1) & 3)));
+        if (dst[i] >= 0 && col + 8 * ch + 8 <= p.cols)
+          *reinterpret_cast<uint4*>(p.out + dst[i] * p.cols + col + 8 * ch) = v;
       }
+      __syncwarp();
     });
   }
 };
 
 // Backward: dH += dZ_chunk W_chunk; fp32 running sum across chunks, bf16 at the end.
+// The running sum's values for the next slice are loaded while the current one is
+// added, so the read-modify-write costs one memory latency per tile, not per slice.
 struct EpiDh {
   using Params = EpiDhParams;
   struct State {};
   __device__ static void unit_begin(const Params&, State&) {}
   __device__ static void unit_end(const Params&, State&, int64_t, int, int) {}
-  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h) {
-    const bool row_ok = row < p.N;
-    const int64_t base = (row_ok ? row : 0) * p.Hd;
-    for_each_slice(taddr, h, [&](int c, float(&x)[32]) {
-      const int64_t col = static_cast<int64_t>(nt) * kBN + c * 32;
-      if (!row_ok || col >= p.Hd) return;
+  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h, uint8_t* stage) {
+    const int lane = threadIdx.x & 31;
+    const int64_t mine = row < p.N ? row : -1;
+    // step i moves rows 4i .. 4i+3 of the warp: lane -> row 4i + lane/8, 4-column chunk lane%8
+    int64_t dst[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int64_t cc = col + 8 * k;
-        if (cc + 8 > p.Hd) continue;
-        float* a = p.acc32 + base + cc;
+    for (int i = 0; i < 8; ++i) dst[i] = __shfl_sync(0xffffffffu, mine, 4 * i + (lane >> 3));
+    const int ch = lane & 7;
+    const int64_t col_tile = static_cast<int64_t>(nt) * kBN;
+    const int c_end = (h + 1) * kSlicesPerWarp;
+    float4 pre[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pre[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto load_sum = [&](int c) {  // this lane's part of slice c of the running sum
+      const int64_t cc = col_tile + c * 32 + 4 * ch;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        pre[i] = (dst[i] >= 0 && cc + 4 <= p.Hd) ? *reinterpret_cast<const float4*>(p.acc32 + dst[i] * p.Hd + cc)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    if (!p.first) load_sum(h * kSlicesPerWarp);
+    for_each_slice(taddr, h, [&](int c, float(&x)[32]) {
+      const int64_t col = col_tile + c * 32;
+      if (col >= p.Hd) return;  // same for the whole warp
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<float4*>(stage + lane * 128 + 16 * (k ^ (lane & 7))) =
+            make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+      __syncwarp();
+      float4 cur[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cur[i] = pre[i];
+      if (!p.first && c + 1 < c_end && col + 32 < p.Hd) load_sum(c + 1);
+      const int64_t cc = col + 4 * ch;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + (lane >> 3);
+        float4 v = *reinterpret_cast<const float4*>(stage + rr * 128 + 16 * (ch ^ (rr & 7)));
+        if (dst[i] < 0 || cc + 4 > p.Hd) continue;
         if (!p.first) {
-          const float4 u0 = *reinterpret_cast<const float4*>(a);
-          const float4 u1 = *reinterpret_cast<const float4*>(a + 4);
-          x[8 * k + 0] += u0.x;
-          x[8 * k + 1] += u0.y;
-          x[8 * k + 2] += u0.z;
-          x[8 * k + 3] += u0.w;
-          x[8 * k + 4] += u1.x;
-          x[8 * k + 5] += u1.y;
-          x[8 * k + 6] += u1.z;
-          x[8 * k + 7] += u1.w;
+          v.x += cur[i].x;
+          v.y += cur[i].y;
+          v.z += cur[i].z;
+          v.w += cur[i].w;
         }
         if (p.last) {
-          uint4 v = make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
-                               pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
-          *reinterpret_cast<uint4*>(p.out + base + cc) = v;
+          *reinterpret_cast<uint2*>(p.out + dst[i] * p.Hd + cc) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
         } else {
-          *reinterpret_cast<float4*>(a) = make_float4(x[8 * k], x[8 * k + 1], x[8 * k + 2], x[8 * k + 3]);
-          *reinterpret_cast<float4*>(a + 4) = make_float4(x[8 * k + 4], x[8 * k + 5], x[8 * k + 6], x[8 * k + 7]);
+          *reinterpret_cast<float4*>(p.acc32 + dst[i] * p.Hd + cc) = v;
         }
       }
+      __syncwarp();
     });
   }
 };
@@ -520,6 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;               // TMEM lane quadrant this warp may access
     const int h = (warp - 2) / 4;         // column half of the tile this warp drains
     const int row_in_tile = int(rank) * kBM + q * 32 + lane;
+    uint8_t* epi_stage = smem + kPairStages * kPairStageBytes + kBarrierBytes + 2 * kMaskWords * sizeof(uint32_t) +
+                         (warp - 2) * kEpiStageBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -538,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
-        Epi::tile(ep, st, taddr, row, nt, h);
+        Epi::tile(ep, st, taddr, row, nt, h, epi_stage);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(tempty0_lead + 8 * acc);
