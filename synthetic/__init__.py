@@ -23,10 +23,10 @@ Recipes (one per workload; sizes follow the shapes the pages discuss):
               seed 5.  Used to measure gradient filtering.
 * ``unigram`` the llama3 shape with a unigram prior, standing in for a trained model whose
               logits favour frequent words: feature 0 of every hidden state is 1 and
-              feature 0 of w_v is -1.1 ln(rank(v) + 1), rank(v) being v's rank in the
-              label draw, so softmax of the prior alone is the labels' own Zipf(1.1) law;
-              the other features are the peaked recipe with b = 8 (applied to features
-              1..Hd-1 only).  About 1e-3 of the softmax entries exceed 2^-12, mostly the
+              feature 0 of w_v is -2 ln(rank(v) + 1), rank(v) being v's rank in the
+              label draw (frequent labels have high prior logits); the other features are
+              the peaked recipe with b = 8 (applied to features 1..Hd-1 only).  About
+              2.3e-4 of the softmax entries exceed 2^-12 (~30 per row), mostly the
               frequent words, scattered over the ids by the rank permutation; seed 6.
               Used to measure vocabulary sorting.
 
@@ -165,7 +165,7 @@ WORKLOADS = {
     "packed": Workload("packed", 32768, 3584, 152064, 4, 0.02, "packed", 0.0,
                        n_seq=8, seq_len=4096, n_docs=4),
     "peaked": Workload("peaked", 8192, 4096, 128256, 5, 0.02, "zipf", 0.05, peak=14.0),
-    "unigram": Workload("unigram", 8192, 4096, 128256, 6, 0.02, "zipf", 0.05, peak=8.0, unigram=1.1),
+    "unigram": Workload("unigram", 8192, 4096, 128256, 6, 0.02, "zipf", 0.05, peak=8.0, unigram=2.0),
 }
 
 
