@@ -234,7 +234,7 @@ def run_ours(args, w):
     red = w.reduction
     budget = args.chunk_budget
     ws_bytes = max(F.forward_workspace_size(N, Hd, V),
-                   F.backward_workspace_size(N, Hd, V, budget, args.sort_vocab))
+                   F.backward_workspace_size(N, Hd, V, budget, args.sort_vocab, args.compensated))
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     dH = torch.empty_like(H)
     dW = torch.empty_like(W)
@@ -243,7 +243,8 @@ def run_ours(args, w):
     def step():
         loss, lse, counts, _ = F.flce_forward(H, W, y, w.ignore_index, w.softcap, red, workspace=workspace)
         F.flce_backward(H, W, y, lse, counts, g, w.ignore_index, w.softcap, red, budget, workspace=workspace,
-                        dH=dH, dW=dW, filter_threshold=args.filter_threshold, sort_vocab=args.sort_vocab)
+                        dH=dH, dW=dW, filter_threshold=args.filter_threshold, sort_vocab=args.sort_vocab,
+                        compensated=args.compensated)
         return loss, counts
 
     for _ in range(args.warmup):
@@ -338,7 +339,7 @@ def run_ours(args, w):
             Hx = b[0].detach().requires_grad_(True)
             Wx = b[1].detach().requires_grad_(True)
             loss = F.linear_cross_entropy(Hx, Wx, b[2], w.ignore_index, w.softcap, red, budget, args.filter_threshold,
-                                          args.sort_vocab)
+                                          args.sort_vocab, args.compensated)
             loss.backward()
             freed[i % 2].record(cur)
             used[i % 2] = True
@@ -382,7 +383,7 @@ def run_ours(args, w):
     torch.cuda.reset_peak_memory_stats(dev)
     base = torch.cuda.memory_allocated(dev)
     loss = F.linear_cross_entropy(Hx, Wx, y, w.ignore_index, w.softcap, red, budget, args.filter_threshold,
-                                  args.sort_vocab)
+                                  args.sort_vocab, args.compensated)
     loss.backward()
     torch.cuda.synchronize()
     peak = torch.cuda.max_memory_allocated(dev) - base
@@ -402,9 +403,11 @@ def run_ours(args, w):
                        "parallelism": "dp%d" % ws if ws > 1 else "single",
                        "l2": "inputs larger than L2 (W %.0f MiB > 129 MB); no flush" % (W.numel() * 2 / 2**20),
                        "chunk_budget_bytes": budget or (1 << 30),
-                       "filter_threshold": args.filter_threshold, "sort_vocab": args.sort_vocab},
+                       "filter_threshold": args.filter_threshold, "sort_vocab": args.sort_vocab,
+                       "compensated": args.compensated},
             # flops counted as the exact path's 8*N*Hd*V; a filtered run skips part of it
-            "flops_basis": "8*N*Hd*V" + (" (exact work; filtering skips some)" if args.filter_threshold > 0 else ""),
+            "flops_basis": "8*N*Hd*V" + (" (exact work; filtering skips some)" if args.filter_threshold > 0 else "")
+                           + (" (the compensated mode runs 12*N*Hd*V)" if args.compensated else ""),
             "pct_bf16_peak": 100.0 * flops / (ms * 1e-3) / (peaks["bf16"] * 1e12),
             "pct_bf16_peak_sustained": 100.0 * flops / (ms * 1e-3) / (peaks["bf16_sus"] * 1e12),
             "peak_extra_mb": peak_extra_mb,
@@ -437,6 +440,8 @@ def main():
                     help="gradient filtering threshold (0 = exact backward; e.g. 2**-12 = 0.000244140625)")
     ap.add_argument("--sort-vocab", action="store_true",
                     help="backward walks the vocabulary in mean-logit order (pays with --filter-threshold)")
+    ap.add_argument("--compensated", action="store_true",
+                    help="backward carries dZ's bf16 rounding remainder (twice the dW / dH work)")
     ap.add_argument("--cpu-sample", type=int, default=1024)
     ap.add_argument("--ref-sample", type=int, default=64)
     ap.add_argument("--no-e2e", action="store_true")

@@ -77,7 +77,8 @@ typedef enum flce_reduction {
                                         expected; the access it would index is skipped) */
 
 /* Backward options (bit flags). */
-#define FLCE_BWD_SORT_VOCAB 1u  /* process the vocabulary in sorted order (flce_vocab_order) */
+#define FLCE_BWD_SORT_VOCAB 1u   /* process the vocabulary in sorted order (flce_vocab_order) */
+#define FLCE_BWD_COMPENSATED 2u  /* carry dZ's bf16 rounding remainder into dH and dW */
 
 /* Bytes of scratch that flce_forward needs for these sizes (0 when N == 0 is fine).
    Returns 0 and sets no error for invalid sizes; flce_forward reports those. */
@@ -88,9 +89,10 @@ FLCE_API size_t flce_forward_workspace_size(int64_t N, int64_t Hd, int64_t V);
    accumulator (the latter only when there is more than one chunk), plus one byte per
    64 x 64 block of the chunk for the filtered mode.  With FLCE_BWD_SORT_VOCAB it also
    holds a bf16 [Vc, Hd] copy of the chunk's weight rows in sorted order and the order
-   itself (about 28 bytes per vocabulary row).
-   chunk_budget_bytes bounds the dZ chunk plus that weight copy (0 = default 1 GiB):
-   Vc = budget / (2 N), or budget / (2 N + 2 Hd) when sorting, rounded down to 256.
+   itself (about 28 bytes per vocabulary row); with FLCE_BWD_COMPENSATED a second bf16
+   [N, Vc] chunk (the rounding remainder of dZ).
+   chunk_budget_bytes bounds the dZ chunk(s) plus that weight copy (0 = default 1 GiB):
+   Vc = budget / (2 N, 4 N when compensated, + 2 Hd when sorting), rounded down to 256.
    The same budget and options must be passed to flce_backward.  Unknown option bits:
    returns 0. */
 FLCE_API size_t flce_backward_workspace_size(int64_t N, int64_t Hd, int64_t V, size_t chunk_budget_bytes,
@@ -134,7 +136,16 @@ FLCE_API flce_status flce_forward(const void* H, const void* W, const int64_t* l
  *                survive filtering gather in few blocks and more blocks are skipped
  *                (Liger-CCE blog, §三 "CCE", vocabulary sorting).  The gradients are the
  *                same sums taken in another order; dW rows are written back to their
- *                ids.  Other bits: FLCE_ERR_ARG.
+ *                ids.
+ *                FLCE_BWD_COMPENSATED: each dZ entry d is kept as its bf16 rounding
+ *                hi = bf16(d) plus the rounded remainder lo = bf16(d - hi), and dH and dW
+ *                accumulate both in fp32 (|d - hi - lo| <= 2^-18 |d| instead of 2^-9): the
+ *                part of the gradient that the bf16 rounding would drop is carried along,
+ *                as the compensation term is in Kahan summation (Liger-CCE blog, §三: CCE's
+ *                kahan variants buy precision, and kahan_full_c also leaves the vocabulary
+ *                side unfiltered, for pretraining).  Requires the unfiltered gradient: with
+ *                filter_threshold > 0, FLCE_ERR_ARG.  Twice the dW and dH tensor work.
+ *                Options combine.  Other bits: FLCE_ERR_ARG.
  *   dH           (device) bf16 [N, Hd] (written)
  *   dW           (device) bf16 [V, Hd] (written, every row)
  *   workspace    (device) >= flce_backward_workspace_size(N, Hd, V, chunk_budget_bytes)

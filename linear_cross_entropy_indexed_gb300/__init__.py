@@ -38,6 +38,11 @@ KERNEL_NAMES = {0: "label_dot", 1: "linear_lse", 2: "lse_merge", 3: "reduce", 4:
                 5: "dz", 6: "dw", 7: "dh", 8: "zero", 9: "block_mask", 10: "selftest", 11: "shard_merge",
                 12: "vocab_keys", 13: "vocab_sort", 14: "gather"}
 BWD_SORT_VOCAB = 1
+BWD_COMPENSATED = 2
+
+
+def _options(sort_vocab: bool, compensated: bool) -> int:
+    return (BWD_SORT_VOCAB if sort_vocab else 0) | (BWD_COMPENSATED if compensated else 0)
 
 _lock = threading.Lock()
 _lib = None
@@ -122,8 +127,9 @@ def forward_workspace_size(N: int, Hd: int, V: int) -> int:
     return int(library().flce_forward_workspace_size(N, Hd, V))
 
 
-def backward_workspace_size(N: int, Hd: int, V: int, chunk_budget: int = 0, sort_vocab: bool = False) -> int:
-    return int(library().flce_backward_workspace_size(N, Hd, V, chunk_budget, BWD_SORT_VOCAB if sort_vocab else 0))
+def backward_workspace_size(N: int, Hd: int, V: int, chunk_budget: int = 0, sort_vocab: bool = False,
+                            compensated: bool = False) -> int:
+    return int(library().flce_backward_workspace_size(N, Hd, V, chunk_budget, _options(sort_vocab, compensated)))
 
 
 def vocab_order(H, W, workspace=None):
@@ -190,12 +196,14 @@ def flce_forward(H, W, labels, ignore_index: int = -100, softcap: float = 0.0, r
 
 def flce_backward(H, W, labels, lse, counts, grad_out, ignore_index: int = -100, softcap: float = 0.0,
                   reduction="mean", chunk_budget: int = 0, workspace=None, dH=None, dW=None,
-                  filter_threshold: float = 0.0, sort_vocab: bool = False):
+                  filter_threshold: float = 0.0, sort_vocab: bool = False, compensated: bool = False):
     """One backward call from the saved LSE and counts.  Returns (dH, dW) in bf16.
     filter_threshold > 0 turns on gradient filtering (softmax entries below it, other
     than the target, are dropped and all-zero blocks are skipped): an approximation.
     sort_vocab walks the vocabulary in mean-logit order (see vocab_order), which gathers
-    the surviving entries into fewer blocks; the result is the same sums reordered."""
+    the surviving entries into fewer blocks; the result is the same sums reordered.
+    compensated carries the bf16 rounding remainder of every dZ entry into dH and dW
+    (twice the dW / dH work; exact gradient only, not with filter_threshold > 0)."""
     _check_inputs(H, W, labels)
     red = _reduction(reduction)
     N, Hd = H.shape
@@ -207,11 +215,11 @@ def flce_backward(H, W, labels, lse, counts, grad_out, ignore_index: int = -100,
     with torch.cuda.device(dev):
         dH = dH if dH is not None else torch.empty_like(H)
         dW = dW if dW is not None else torch.empty_like(W)
-        need = backward_workspace_size(N, Hd, V, chunk_budget, sort_vocab)
+        need = backward_workspace_size(N, Hd, V, chunk_budget, sort_vocab, compensated)
         ws = workspace if workspace is not None else torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         _check(library().flce_backward(_p(H), _p(W), _p(labels), _p(lse), _p(counts), N, Hd, V, int(ignore_index),
                                        float(softcap), red, _p(g), float(filter_threshold),
-                                       BWD_SORT_VOCAB if sort_vocab else 0, _p(dH), _p(dW), _p(ws), ws.numel(),
+                                       _options(sort_vocab, compensated), _p(dH), _p(dW), _p(ws), ws.numel(),
                                        int(chunk_budget), _stream(dev)))
     return dH, dW
 
@@ -259,7 +267,7 @@ def flce_merge_shards(lse_parts, target_parts, labels, V_total: int, ignore_inde
 
 def flce_backward_shard(H, W_shard, labels, lse, counts, grad_out, v_offset: int, V_total: int,
                         ignore_index: int = -100, softcap: float = 0.0, reduction="mean", chunk_budget: int = 0,
-                        filter_threshold: float = 0.0, sort_vocab: bool = False):
+                        filter_threshold: float = 0.0, sort_vocab: bool = False, compensated: bool = False):
     """Backward over one vocabulary shard from the global lse and counts.  Returns
     (dH_partial fp32 [N, Hd], to be summed over the shards; dW_shard bf16)."""
     _check_inputs(H, W_shard, labels)
@@ -271,11 +279,11 @@ def flce_backward_shard(H, W_shard, labels, lse, counts, grad_out, v_offset: int
     with torch.cuda.device(dev):
         dh = torch.empty(N, Hd, dtype=torch.float32, device=dev)
         dw = torch.empty_like(W_shard)
-        need = backward_workspace_size(N, Hd, Vs, chunk_budget, sort_vocab)
+        need = backward_workspace_size(N, Hd, Vs, chunk_budget, sort_vocab, compensated)
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         _check(library().flce_backward_shard(_p(H), _p(W_shard), _p(labels), _p(lse), _p(counts), N, Hd, Vs,
                                              int(v_offset), int(V_total), int(ignore_index), float(softcap), red,
-                                             _p(g), float(filter_threshold), BWD_SORT_VOCAB if sort_vocab else 0,
+                                             _p(g), float(filter_threshold), _options(sort_vocab, compensated),
                                              _p(dh), _p(dw), _p(ws), ws.numel(), int(chunk_budget), _stream(dev)))
     return dh, dw
 
@@ -294,36 +302,38 @@ def check_counts(counts) -> tuple[int, int]:
 
 class _FusedLinearCrossEntropy(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, H, W, labels, ignore_index, softcap, reduction, chunk_budget, filter_threshold, sort_vocab):
+    def forward(ctx, H, W, labels, ignore_index, softcap, reduction, chunk_budget, filter_threshold, sort_vocab,
+                compensated):
         loss, lse, counts, _ = flce_forward(H, W, labels, ignore_index, softcap, reduction)
         ctx.save_for_backward(H, W, labels, lse, counts)
-        ctx.cfg = (ignore_index, softcap, reduction, chunk_budget, filter_threshold, sort_vocab)
+        ctx.cfg = (ignore_index, softcap, reduction, chunk_budget, filter_threshold, sort_vocab, compensated)
         return loss
 
     @staticmethod
     def backward(ctx, grad):
         H, W, labels, lse, counts = ctx.saved_tensors
-        ignore_index, softcap, reduction, chunk_budget, filter_threshold, sort_vocab = ctx.cfg
+        ignore_index, softcap, reduction, chunk_budget, filter_threshold, sort_vocab, compensated = ctx.cfg
         dH, dW = flce_backward(H, W, labels, lse, counts, grad, ignore_index, softcap, reduction, chunk_budget,
-                               filter_threshold=filter_threshold, sort_vocab=sort_vocab)
+                               filter_threshold=filter_threshold, sort_vocab=sort_vocab, compensated=compensated)
         return (dH if ctx.needs_input_grad[0] else None, dW if ctx.needs_input_grad[1] else None,
-                None, None, None, None, None, None, None)
+                None, None, None, None, None, None, None, None)
 
 
 def linear_cross_entropy(hidden, weight, labels, ignore_index: int = -100, softcap: float = 0.0,
                          reduction: str = "mean", chunk_budget: int = 0, filter_threshold: float = 0.0,
-                         sort_vocab: bool = False):
+                         sort_vocab: bool = False, compensated: bool = False):
     """Cross-entropy of ``hidden @ weight.T`` against ``labels`` without materialising
     the logits.  ``hidden`` [..., Hd] bf16, ``weight`` [V, Hd] bf16, ``labels`` [...]
     int64.  reduction: "mean" (over rows whose label is valid), "sum" or "none".
-    filter_threshold > 0 (e.g. 2**-12) makes the backward approximate, and sort_vocab
-    lets it skip more blocks: see flce_backward."""
+    filter_threshold > 0 (e.g. 2**-12) makes the backward approximate, sort_vocab lets it
+    skip more blocks, compensated makes the exact backward more precise: see
+    flce_backward."""
     Hd = hidden.shape[-1]
     H2 = hidden.reshape(-1, Hd)
     y = labels.reshape(-1)
     out = _FusedLinearCrossEntropy.apply(H2.contiguous(), weight.contiguous(), y.contiguous(), int(ignore_index),
                                          float(softcap), reduction, int(chunk_budget), float(filter_threshold),
-                                         bool(sort_vocab))
+                                         bool(sort_vocab), bool(compensated))
     if reduction == "none":
         out = out.reshape(labels.shape)
     return out
@@ -340,7 +350,8 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
     """
 
     def __init__(self, ignore_index: int = -100, softcap: float = 0.0, reduction: str = "mean",
-                 chunk_budget: int = 0, filter_threshold: float = 0.0, sort_vocab: bool = False):
+                 chunk_budget: int = 0, filter_threshold: float = 0.0, sort_vocab: bool = False,
+                 compensated: bool = False):
         super().__init__()
         _reduction(reduction)
         self.ignore_index = int(ignore_index)
@@ -349,14 +360,15 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
         self.chunk_budget = int(chunk_budget)
         self.filter_threshold = float(filter_threshold)
         self.sort_vocab = bool(sort_vocab)
+        self.compensated = bool(compensated)
 
     def forward(self, weight, hidden, labels):
         return linear_cross_entropy(hidden, weight, labels, self.ignore_index, self.softcap, self.reduction,
-                                    self.chunk_budget, self.filter_threshold, self.sort_vocab)
+                                    self.chunk_budget, self.filter_threshold, self.sort_vocab, self.compensated)
 
     def extra_repr(self):
-        return "ignore_index=%d, softcap=%g, reduction=%s, filter_threshold=%g, sort_vocab=%s" % (
-            self.ignore_index, self.softcap, self.reduction, self.filter_threshold, self.sort_vocab)
+        return "ignore_index=%d, softcap=%g, reduction=%s, filter_threshold=%g, sort_vocab=%s, compensated=%s" % (
+            self.ignore_index, self.softcap, self.reduction, self.filter_threshold, self.sort_vocab, self.compensated)
 
 
 def launch_count() -> int:

@@ -239,21 +239,24 @@ struct BwdPlan {
   int n_chunks = 0;
   int nz_rows = 0, nz_ld = 0;  // token blocks x vocabulary blocks of the dZ block flags
   int dh_mask_ld = 0, dw_mask_ld = 0, mask_tok_tiles = 0, mask_voc_tiles = 0;
-  bool sort = false;
+  bool sort = false, split = false;
   VocabPlan vocab;
-  size_t off_rows = 0, off_dz = 0, off_dh = 0, off_nz = 0, off_dh_mask = 0, off_dw_mask = 0, off_wperm = 0, total = 0;
+  size_t off_rows = 0, off_dz = 0, off_dz_lo = 0, off_dh = 0, off_nz = 0, off_dh_mask = 0, off_dw_mask = 0,
+         off_wperm = 0, total = 0;
 };
 
-// The chunk budget covers the bf16 dZ chunk and, with the sorted vocabulary, the bf16
-// copy of the chunk's weight rows in sorted order: Vc = budget / (2N (+ 2Hd)).
+// The chunk budget covers the bf16 dZ chunk (two of them, value and rounding remainder, in
+// the compensated mode) and, with the sorted vocabulary, the bf16 copy of the chunk's
+// weight rows in sorted order: Vc = budget / (2N (x2) (+ 2Hd)).
 flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, unsigned options, BwdPlan* p) {
   flce_status s = check_sizes(N, Hd, V);
   if (s != FLCE_OK) return s;
-  if ((options & ~unsigned(FLCE_BWD_SORT_VOCAB)) != 0) return FLCE_ERR_ARG;
+  if ((options & ~unsigned(FLCE_BWD_SORT_VOCAB | FLCE_BWD_COMPENSATED)) != 0) return FLCE_ERR_ARG;
   p->sort = (options & FLCE_BWD_SORT_VOCAB) != 0;
+  p->split = (options & FLCE_BWD_COMPENSATED) != 0;
   if (budget == 0) budget = kDefaultChunkBudget;
   const int64_t v_round = int64_t(cdiv(V, kBN)) * kBN;
-  const size_t per_col = size_t(N) * 2 + (p->sort ? size_t(Hd) * 2 : 0);
+  const size_t per_col = size_t(N) * (p->split ? 4 : 2) + (p->sort ? size_t(Hd) * 2 : 0);
   int64_t vc = N > 0 ? static_cast<int64_t>(budget / per_col) : v_round;
   vc = vc / kBN * kBN;
   if (vc < kBN) vc = kBN;
@@ -270,6 +273,7 @@ flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, unsig
   if (!mul_ok(size_t(N), size_t(vc), &dz) || !mul_ok(dz, 2, &dz)) return FLCE_ERR_OVERFLOW;
   if (p->n_chunks > 1 && (!mul_ok(size_t(N), size_t(Hd), &dh) || !mul_ok(dh, 4, &dh))) return FLCE_ERR_OVERFLOW;
   if (!reserve(&cur, size_t(N) * sizeof(RowInfo), &p->off_rows) || !reserve(&cur, dz, &p->off_dz) ||
+      !reserve(&cur, p->split ? dz : 0, &p->off_dz_lo) ||
       !reserve(&cur, dh, &p->off_dh) || !reserve(&cur, size_t(p->nz_rows) * size_t(p->nz_ld), &p->off_nz) ||
       !reserve(&cur, size_t(p->mask_tok_tiles) * p->dh_mask_ld * 4, &p->off_dh_mask) ||
       !reserve(&cur, size_t(p->mask_voc_tiles) * p->dw_mask_ld * 4, &p->off_dw_mask))
@@ -436,6 +440,7 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
                           size_t workspace_bytes, size_t chunk_budget_bytes, void* stream) {
   if (reduction < 0 || reduction > 2 || softcap != softcap || !(filter_threshold >= 0.0f)) return FLCE_ERR_ARG;
   const bool filter = filter_threshold > 0.0f;
+  if (filter && (options & FLCE_BWD_COMPENSATED) != 0) return FLCE_ERR_ARG;  // exact gradients only
   BwdPlan pl;
   flce_status s = plan_backward(N, Hd, V, chunk_budget_bytes, options, &pl);
   if (s != FLCE_OK) return s;
@@ -459,6 +464,7 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   RowInfo* rows = reinterpret_cast<RowInfo*>(ws + pl.off_rows);
   __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_dz);
+  __nv_bfloat16* dz_lo = pl.split ? reinterpret_cast<__nv_bfloat16*>(ws + pl.off_dz_lo) : nullptr;
   float* dh32 = pl.n_chunks > 1 ? reinterpret_cast<float*>(ws + pl.off_dh) : nullptr;
   uint8_t* nz = filter ? ws + pl.off_nz : nullptr;
   uint32_t* dh_mask = reinterpret_cast<uint32_t*>(ws + pl.off_dh_mask);
@@ -498,9 +504,16 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
   for (int c = 0; c < pl.n_chunks; ++c) {
     const int64_t v0 = int64_t(c) * pl.Vc;
     const int64_t wc = std::min<int64_t>(pl.Vc, V - v0);
-    CUtensorMap tmDz_k, tmDz_mn;
+    CUtensorMap tmDz_k, tmDz_mn, tmLo_k, tmLo_mn;
     if (!tmap_2d(&tmDz_k, dz, wc, N, pl.Vc * 2, kBK, kBM) || !tmap_2d(&tmDz_mn, dz, wc, N, pl.Vc * 2, 64, kBK))
       return FLCE_ERR_CUDA;
+    if (pl.split) {
+      if (!tmap_2d(&tmLo_k, dz_lo, wc, N, pl.Vc * 2, kBK, kBM) || !tmap_2d(&tmLo_mn, dz_lo, wc, N, pl.Vc * 2, 64, kBK))
+        return FLCE_ERR_CUDA;
+    } else {
+      tmLo_k = tmDz_k;
+      tmLo_mn = tmDz_mn;
+    }
     int64_t w_off = v0;  // first weight row of the chunk in the tensor maps
     if (pl.sort) {
       e = launch(FLCE_KERNEL_GATHER, st, [&] {
@@ -526,7 +539,7 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
     s4.b_n_off = static_cast<int>(w_off);
     if (filter && (e = cudaMemsetAsync(nz, 0, size_t(pl.nz_rows) * size_t(pl.nz_ld), st)) != cudaSuccess)
       return cuda_fail(e);
-    EpiDzParams p4{N, V, v0, wc, pl.Vc, softcap, rows, dz, filter_threshold, nz, pl.nz_ld};
+    EpiDzParams p4{N, V, v0, wc, pl.Vc, softcap, rows, dz, dz_lo, filter_threshold, nz, pl.nz_ld};
     e = launch(FLCE_KERNEL_DZ, st,
                [&] { return launch_dz(tmH_k, tmW_k, s4, p4, err, pair_grid(s4.units, sms), st); });
     if (e != cudaSuccess) return cuda_fail(e);
@@ -556,9 +569,13 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
       s5.kmask = dw_mask;
       s5.kmask_ld = pl.dw_mask_ld;
     }
+    if (pl.split) {  // dZ^T H + dZ_lo^T H in one accumulator
+      s5.k_half = s5.k_blocks;
+      s5.k_blocks *= 2;
+    }
     EpiDwParams p5{wc, v0, Hd, static_cast<__nv_bfloat16*>(dW), perm, V};
     e = launch(FLCE_KERNEL_DW, st,
-               [&] { return launch_dw(tmDz_mn, tmH_mn, s5, p5, err, pair_grid(s5.units, sms), st); });
+               [&] { return launch_dw(tmDz_mn, tmLo_mn, tmH_mn, s5, p5, err, pair_grid(s5.units, sms), st); });
     if (e != cudaSuccess) return cuda_fail(e);
 
     // dH (+)= dZ_chunk W_chunk
@@ -575,11 +592,15 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
       s6.kmask = dh_mask;
       s6.kmask_ld = pl.dh_mask_ld;
     }
+    if (pl.split) {  // dZ W + dZ_lo W in one accumulator
+      s6.k_half = s6.k_blocks;
+      s6.k_blocks *= 2;
+    }
     EpiDhParams p6 = dh_partial != nullptr
                          ? EpiDhParams{N, Hd, dh_partial, nullptr, c == 0, 0}
                          : EpiDhParams{N, Hd, dh32, static_cast<__nv_bfloat16*>(dH), c == 0, c == pl.n_chunks - 1};
     e = launch(FLCE_KERNEL_DH, st,
-               [&] { return launch_dh(tmDz_k, tmW_mn, s6, p6, err, pair_grid(s6.units, sms), st); });
+               [&] { return launch_dh(tmDz_k, tmLo_k, tmW_mn, s6, p6, err, pair_grid(s6.units, sms), st); });
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return FLCE_OK;

@@ -9,17 +9,17 @@ namespace flce {
 
 cudaError_t launch_dz(const CUtensorMap& tmH, const CUtensorMap& tmW, const Sched& s,
                       const EpiDzParams& p, unsigned long long* err, int grid, cudaStream_t st) {
-  return launch_gemm<EpiDz, false, false>(tmH, tmW, s, p, err, grid, st);
+  return launch_gemm<EpiDz, false, false>(tmH, tmH, tmW, s, p, err, grid, st);
 }
 
-cudaError_t launch_dw(const CUtensorMap& tmDz, const CUtensorMap& tmH, const Sched& s,
+cudaError_t launch_dw(const CUtensorMap& tmDz, const CUtensorMap& tmDz2, const CUtensorMap& tmH, const Sched& s,
                       const EpiDwParams& p, unsigned long long* err, int grid, cudaStream_t st) {
-  return launch_gemm<EpiDw, true, true>(tmDz, tmH, s, p, err, grid, st);
+  return launch_gemm<EpiDw, true, true>(tmDz, tmDz2, tmH, s, p, err, grid, st);
 }
 
-cudaError_t launch_dh(const CUtensorMap& tmDz, const CUtensorMap& tmW, const Sched& s,
+cudaError_t launch_dh(const CUtensorMap& tmDz, const CUtensorMap& tmDz2, const CUtensorMap& tmW, const Sched& s,
                       const EpiDhParams& p, unsigned long long* err, int grid, cudaStream_t st) {
-  return launch_gemm<EpiDh, false, true>(tmDz, tmW, s, p, err, grid, st);
+  return launch_gemm<EpiDh, false, true>(tmDz, tmDz2, tmW, s, p, err, grid, st);
 }
 
 cudaError_t set_gemm_smem_attributes_bwd() {

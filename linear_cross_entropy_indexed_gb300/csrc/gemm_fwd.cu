@@ -8,7 +8,7 @@ namespace flce {
 cudaError_t launch_linear_lse(const CUtensorMap& tmH, const CUtensorMap& tmW, const Sched& s,
                               const EpiLseParams& p, unsigned long long* err, int grid,
                               cudaStream_t st) {
-  return launch_gemm<EpiLse, false, false>(tmH, tmW, s, p, err, grid, st);
+  return launch_gemm<EpiLse, false, false>(tmH, tmH, tmW, s, p, err, grid, st);
 }
 
 cudaError_t set_gemm_smem_attributes_fwd() { return set_smem_attr<EpiLse, false, false>(); }

@@ -52,6 +52,10 @@ struct Sched {
   // A K step whose slab is all zero is neither loaded nor multiplied.
   const uint32_t* kmask;
   int kmask_ld;
+  // Two-part A operand (0: off): K steps [0, k_half) read A through the first tensor map,
+  // steps [k_half, 2 k_half) the same coordinates through the second; B is read at the
+  // step index modulo k_half, so the accumulator sums A1 B + A2 B.
+  int k_half;
 };
 
 // Per-row data the dZ epilogue needs, packed in one 16-byte load.
@@ -77,6 +81,7 @@ struct EpiDzParams {
   float softcap;
   const RowInfo* rows;
   __nv_bfloat16* dz;
+  __nv_bfloat16* dz_lo;  // compensated mode: bf16 rounding remainder of dZ (same layout), else null
   float filter;         // drop entries with p < filter off the target (0: exact)
   uint8_t* nz;          // block flags written when filtering, else null
   int nz_ld;            // vocabulary blocks per token-block row of nz
@@ -104,9 +109,10 @@ cudaError_t launch_linear_lse(const CUtensorMap& tmH, const CUtensorMap& tmW, co
                               cudaStream_t st);
 cudaError_t launch_dz(const CUtensorMap& tmH, const CUtensorMap& tmW, const Sched& s,
                       const EpiDzParams& p, unsigned long long* err, int grid, cudaStream_t st);
-cudaError_t launch_dw(const CUtensorMap& tmDz, const CUtensorMap& tmH, const Sched& s,
+// tmDz2: second part of the A operand when s.k_half > 0 (see Sched), else unused.
+cudaError_t launch_dw(const CUtensorMap& tmDz, const CUtensorMap& tmDz2, const CUtensorMap& tmH, const Sched& s,
                       const EpiDwParams& p, unsigned long long* err, int grid, cudaStream_t st);
-cudaError_t launch_dh(const CUtensorMap& tmDz, const CUtensorMap& tmW, const Sched& s,
+cudaError_t launch_dh(const CUtensorMap& tmDz, const CUtensorMap& tmDz2, const CUtensorMap& tmW, const Sched& s,
                       const EpiDhParams& p, unsigned long long* err, int grid, cudaStream_t st);
 cudaError_t set_gemm_smem_attributes_fwd();
 cudaError_t set_gemm_smem_attributes_bwd();

@@ -140,7 +140,7 @@ struct EpiDz {
   struct State {};
   __device__ static void unit_begin(const Params&, State&) {}
   __device__ static void unit_end(const Params&, State&, int64_t, int, int) {}
-  template <bool CAP, bool FILTER>
+  template <bool CAP, bool FILTER, bool SPLIT>
   __device__ static void slices(const Params& p, uint32_t taddr, int64_t row, int nt, int h) {
     RowInfo ri{0.0f, 0.0f, -1, 0};
     const bool row_ok = row < p.N;
@@ -151,11 +151,13 @@ struct EpiDz {
     const int64_t vl_tile = static_cast<int64_t>(nt) * kBN;
     const int64_t y_local = ri.label >= 0 ? static_cast<int64_t>(ri.label) - p.v0 : -1;
     __nv_bfloat16* out_row = p.dz + (row_ok ? row : 0) * p.ldz;
+    __nv_bfloat16* lo_row = SPLIT ? p.dz_lo + (row_ok ? row : 0) * p.ldz : nullptr;
     for_each_slice(taddr, h, [&](int c, float(&x)[32]) {
       const int64_t vl = vl_tile + c * 32;
       if (vl >= p.wc) return;  // same for the whole warp
       const int yrel = (y_local >= vl && y_local < vl + 32) ? static_cast<int>(y_local - vl) : -1;
       uint32_t pk[16];
+      uint32_t pl[SPLIT ? 16 : 1];
       bool nonzero = false;
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
@@ -178,6 +180,11 @@ struct EpiDz {
           d[e] = dv;
         }
         pk[j / 2] = pack_bf16x2(d[0], d[1]);
+        if (SPLIT) {  // remainder of the bf16 rounding, itself rounded to bf16
+          const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&pk[j / 2]);
+          const float2 hf = __bfloat1622float2(hb);
+          pl[j / 2] = pack_bf16x2(d[0] - hf.x, d[1] - hf.y);
+        }
       }
       if (FILTER) {
         const unsigned any = __ballot_sync(0xffffffffu, nonzero && row_ok);
@@ -188,27 +195,41 @@ struct EpiDz {
         uint4* dst = reinterpret_cast<uint4*>(out_row + vl);
 #pragma unroll
         for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        if (SPLIT) {
+          uint4* dlo = reinterpret_cast<uint4*>(lo_row + vl);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) dlo[k] = make_uint4(pl[4 * k], pl[4 * k + 1], pl[4 * k + 2], pl[4 * k + 3]);
+        }
       } else {
         for (int j = 0; j < 32 && vl + j < p.wc; ++j) {
           const uint32_t w = pk[j / 2];
           const uint16_t hbits = static_cast<uint16_t>((j & 1) ? (w >> 16) : (w & 0xFFFFu));
           reinterpret_cast<uint16_t*>(out_row)[vl + j] = hbits;
+          if (SPLIT) {
+            const uint32_t wl = pl[j / 2];
+            reinterpret_cast<uint16_t*>(lo_row)[vl + j] = static_cast<uint16_t>((j & 1) ? (wl >> 16) : (wl & 0xFFFFu));
+          }
         }
       }
     });
   }
   __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h, uint8_t*) {
     const bool cap = p.softcap > 0.0f;
-    if (p.nz != nullptr) {
+    if (p.nz != nullptr) {  // filtering (the backward never combines it with the split)
       if (cap)
-        slices<true, true>(p, taddr, row, nt, h);
+        slices<true, true, false>(p, taddr, row, nt, h);
       else
-        slices<false, true>(p, taddr, row, nt, h);
+        slices<false, true, false>(p, taddr, row, nt, h);
+    } else if (p.dz_lo != nullptr) {
+      if (cap)
+        slices<true, false, true>(p, taddr, row, nt, h);
+      else
+        slices<false, false, true>(p, taddr, row, nt, h);
     } else {
       if (cap)
-        slices<true, false>(p, taddr, row, nt, h);
+        slices<true, false, false>(p, taddr, row, nt, h);
       else
-        slices<false, false>(p, taddr, row, nt, h);
+        slices<false, false, false>(p, taddr, row, nt, h);
     }
   }
 };
@@ -379,7 +400,8 @@ __device__ __forceinline__ void load_half_pair(uint32_t dst, const CUtensorMap* 
 
 template <class Epi, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                   const __grid_constant__ CUtensorMap tmB,
                         const Sched sched, const typename Epi::Params ep, unsigned long long* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -415,6 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
+    if (sched.k_half > 0) tma_prefetch_desc(&tmA2);
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
@@ -442,13 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nt0 = g * sched.group;
         const int nt1 = min(nt0 + sched.group, sched.n_tiles);
         for (int nt = nt0; ok && nt < nt1; ++nt) {
-          // one K step: wait for a free slot, arm the full barrier, load both halves
-          auto load_step = [&](int kb) -> bool {
+          // one K step: wait for a free slot, arm the full barrier, load both halves of A
+          // (through map ta) and of B, at K block kb
+          auto load_k = [&](const CUtensorMap* ta, int kb) -> bool {
             if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, err)) return false;
             if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * kPairStageBytes);
             const uint32_t a = tiles_u32 + stage * kPairStageBytes;
             const uint32_t fb = full0_lead + 8 * stage;
-            load_half_pair<A_MN>(a, &tmA, fb, mt * kPairM + int(rank) * kBM, kb * kBK);
+            load_half_pair<A_MN>(a, ta, fb, mt * kPairM + int(rank) * kBM, kb * kBK);
             load_half_pair<B_MN>(a + kATileBytes, &tmB, fb, nt * kBN + int(rank) * kPairBRows + sched.b_n_off,
                                  kb * kBK + sched.b_k_off);
             armed |= 1u << stage;
@@ -459,12 +483,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return true;
           };
-          if (sched.kmask == nullptr) {
+          auto load_step = [&](int kb) -> bool { return load_k(&tmA, kb); };
+          if (sched.kmask == nullptr && sched.k_half == 0) {
             for (int kb = 0; kb < sched.k_blocks; ++kb)
               if (!load_step(kb)) {
                 ok = false;
                 break;
               }
+          } else if (sched.kmask == nullptr) {  // two-part A: A1 B over all K blocks, then A2 B
+            for (int kb = 0; kb < sched.k_blocks; ++kb) {
+              const bool second = kb >= sched.k_half;
+              if (!load_k(second ? &tmA2 : &tmA, second ? kb - sched.k_half : kb)) {
+                ok = false;
+                break;
+              }
+            }
           } else {  // filtered dZ: only the K steps of the tile's mask
             uint32_t* mask = kmask;
             load_kmask(sched, mt, mask);
@@ -606,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <class Epi, bool A_MN, bool B_MN>
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Sched& s,
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmA2, const CUtensorMap& tmB, const Sched& s,
                              const typename Epi::Params& p, unsigned long long* err, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
@@ -620,7 +653,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Sc
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<Epi, A_MN, B_MN>, tmA, tmB, s, p, err);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<Epi, A_MN, B_MN>, tmA, tmA2, tmB, s, p, err);
 }
 
 template <class Epi, bool A_MN, bool B_MN>

@@ -44,7 +44,7 @@ def make_case(w: S.Workload, labels: np.ndarray | None = None):
 
 
 def run_gpu(Hb, Wb, y, ignore_index=-100, softcap=0.0, reduction="mean", grad=None, chunk_budget=0,
-            backward=True, filter_threshold=0.0, sort_vocab=False):
+            backward=True, filter_threshold=0.0, sort_vocab=False, compensated=False):
     import linear_cross_entropy_indexed_gb300 as F
     H = to_device(Hb)
     W = to_device(Wb)
@@ -58,7 +58,7 @@ def run_gpu(Hb, Wb, y, ignore_index=-100, softcap=0.0, reduction="mean", grad=No
             grad = np.linspace(0.5, 1.5, N) if reduction == "none" else np.array([1.0])
         g = torch.tensor(np.asarray(grad, dtype=np.float32)).cuda()
         dH, dW = F.flce_backward(H, W, lab, lse, counts, g, ignore_index, softcap, reduction, chunk_budget,
-                                 filter_threshold=filter_threshold, sort_vocab=sort_vocab)
+                                 filter_threshold=filter_threshold, sort_vocab=sort_vocab, compensated=compensated)
         out["dH"] = S.bf16_bits_to_f32(bf16_bits(dH)).astype(np.float64)
         out["dW"] = S.bf16_bits_to_f32(bf16_bits(dW)).astype(np.float64)
         out["counts_after"] = counts.cpu().numpy()

@@ -78,7 +78,12 @@ def test_workspace_sizes(lib):
     size_s = b(n, hd, v, budget, 1)
     base = n * vs * 2 + vs * hd * 2 + n * hd * 4 + n * 16 + flags_s + 28 * v + 128 * hd * 4 + hd * 4
     assert base <= size_s < base + (1 << 13)
-    assert b(n, hd, v, budget, 2) == 0 and b(n, hd, v, budget, 0x80000000) == 0
+    assert b(n, hd, v, budget, 4) == 0 and b(n, hd, v, budget, 0x80000000) == 0
+    # compensated: two bf16 dZ chunks, Vc = budget / 4N
+    vcc = (budget // (4 * n)) // 256 * 256
+    size_c = b(n, hd, v, budget, 2)
+    base_c = 2 * n * vcc * 2 + n * hd * 4 + n * 16 + (n // 64) * (vcc // 64)
+    assert base_c <= size_c < base_c + (1 << 13)
     o = lib.flce_vocab_order_workspace_size
     assert 28 * v + 128 * hd * 4 + hd * 4 <= o(n, hd, v) < 28 * v + 128 * hd * 4 + hd * 4 + (1 << 12)
     assert o(0, 64, 10) > 0 and o(8, 60, 10) == 0 and o(8, 64, 0) == 0
@@ -112,7 +117,8 @@ def test_argument_errors_before_any_device_work(lib):
     assert _bwd(lib, dW=None) == ARG
     assert _bwd(lib, ws_bytes=16) == WS
     assert _bwd(lib, W=0x2002) == ALIGN
-    assert _bwd(lib, options=2) == ARG
+    assert _bwd(lib, options=4) == ARG
+    assert _bwd(lib, options=2, filt=0.25) == ARG  # the compensated mode is exact-only
     assert _bwd(lib, options=1, ws_bytes=lib.flce_backward_workspace_size(16, 64, 100, 0, 0)) == WS
     vo = lambda H=0x1000, W=0x2000, perm=0x3000, ws_bytes=1 << 20, Hd=64: lib.flce_vocab_order(
         H, W, 16, Hd, 100, None, perm, None, 0x10000, ws_bytes, None)
