@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kRowCopyThreads)
   for (int64_t v = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; v < V; v += n_warps) {
     const __nv_bfloat16* w = W + v * Hd;
     float acc = 0.0f;
-#pragma unroll 4
+#pragma unroll 8
     for (int64_t c = lane * 8; c < Hd; c += 256) {
       const uint4 q = __ldg(reinterpret_cast<const uint4*>(w + c));
       const float4 h0 = __ldg(reinterpret_cast<const float4*>(hbar + c));
