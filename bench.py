@@ -290,8 +290,11 @@ def run_ours(args, w):
         c = per_class.setdefault(name, [0, 0.0])
         c[0] += 1
         c[1] += d
-    flops_per_class = {"linear_lse": 2.0 * N * Hd * V, "dz": 2.0 * N * Hd * V, "dw": 2.0 * N * Hd * V,
-                       "dh": 2.0 * N * Hd * V}  # per step, summed over that class's launches
+    # per step, summed over that class's launches; the compensated backward multiplies both
+    # the bf16 value and the rounding remainder of dZ, twice the dW and dH products
+    prod = 4.0 if args.compensated else 2.0
+    flops_per_class = {"linear_lse": 2.0 * N * Hd * V, "dz": 2.0 * N * Hd * V, "dw": prod * N * Hd * V,
+                       "dh": prod * N * Hd * V}
     dom = max(per_class, key=lambda k: per_class[k][1])
     roof = None
     if dom in flops_per_class:
