@@ -34,9 +34,13 @@ L2_BYTES = 129 * 10**6
 # DRAM traffic per launch of the dominant kernel class from one ncu capture, keyed by
 # the hash of the kernel sources it was taken on (null once the sources change).
 MEASURED_TRAFFIC = {
-    # ncu capture of the dZ kernel at the llama2 size (1.833 GB read + 0.513 GB written
-    # per launch), scaled by tiles per launch to llama3 (x 2.004)
-    ("dz", "llama3", "68cd6ff828a14463"): 4.70e9,
+    # ncu capture of the four tensor-core kernels at the llama2 size (DRAM read + written
+    # per launch), scaled by tiles per launch to llama3: x 4.008 for the linear-LSE launch
+    # (501 / 125 vocabulary tiles), x 2.004 for the per-chunk dZ / dW / dH launches
+    ("linear_lse", "llama3", "fa8d48f5b9b0d8fa"): 3.95e9,   # 0.981 + 0.005 GB at llama2
+    ("dz", "llama3", "fa8d48f5b9b0d8fa"): 4.64e9,           # 1.805 + 0.512 GB
+    ("dw", "llama3", "fa8d48f5b9b0d8fa"): 5.16e9,           # 2.316 + 0.257 GB
+    ("dh", "llama3", "fa8d48f5b9b0d8fa"): 5.15e9,           # 2.507 + 0.063 GB
 }
 
 
