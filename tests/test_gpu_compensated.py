@@ -126,3 +126,17 @@ def test_full_size_llama3_compensated():
         e[False] + e[True] + floors))
     _check(dict(dH_err=e[False][0], dW_err=e[False][1]), dict(dH_err=e[True][0], dW_err=e[True][1]), floors)
     assert max(e[True]) <= P.TOL_GRAD_FRO
+
+
+def test_compensated_all_ignored_and_bad_labels():
+    w = S.scaled("tiny", N=130, Hd=64, V=700, seed=86)
+    Hb, Wb, y = P.make_case(w)
+    y = np.full(130, -100, dtype=np.int64)
+    out = P.run_gpu(Hb, Wb, y, compensated=True)
+    assert np.abs(out["dH"]).max() == 0.0 and np.abs(out["dW"]).max() == 0.0
+    y = S.make_labels(w)
+    y[0] = 700
+    out = P.run_gpu(Hb, Wb, y, compensated=True, reduction="sum")
+    ref, dH, dW = P.oracle_full(Hb, Wb, y, reduction="sum")
+    P.check_backward(out, dH, dW)
+    assert int(out["counts"][1]) == 1 and np.abs(out["dH"][0]).max() == 0.0

@@ -178,3 +178,29 @@ def test_full_size_unigram_order_and_sorted_gradients():
         P.fro_rel(dh_got, dh_ref), P.fro_rel(dw_got, dw_ref)))
     assert P.fro_rel(dh_got, dh_ref) <= P.TOL_GRAD_FRO
     assert P.fro_rel(dw_got, dw_ref) <= P.TOL_GRAD_FRO
+
+
+def test_sorted_with_bad_labels_and_custom_ignore_index():
+    """Labels are mapped to positions only when valid: out-of-range and ignored rows keep no
+    one-hot and no gradient under the sorted walk."""
+    w = S.scaled("unigram", N=200, Hd=64, V=3000, seed=79)
+    Hb, Wb, y = P.make_case(w)
+    y = y.copy()
+    y[y == -100] = 7          # 7 becomes the ignore index
+    y[3] = 3000               # out of range
+    y[4] = -5                 # negative, not the ignore index
+    out = P.run_gpu(Hb, Wb, y, 7, 0.0, "sum", filter_threshold=THR, sort_vocab=True, chunk_budget=(2 * 200 + 2 * 64) * 1024)
+    ref, dH, dW = P.oracle_full(Hb, Wb, y, 7, 0.0, "sum", filter_threshold=THR)
+    P.check_forward(out, ref, y, w.V, 7, "sum")
+    P.check_backward(out, dH, dW)
+    assert int(out["counts"][1]) == 2
+    assert np.abs(out["dH"][[3, 4]]).max() == 0.0
+
+
+def test_sorted_all_ignored_is_zero():
+    w = S.scaled("tiny", N=150, Hd=64, V=900, seed=80)
+    Hb, Wb, _ = P.make_case(w)
+    y = np.full(150, -100, dtype=np.int64)
+    out = P.run_gpu(Hb, Wb, y, sort_vocab=True)
+    assert np.abs(out["dH"]).max() == 0.0 and np.abs(out["dW"]).max() == 0.0
+    assert int(out["counts_after"][2]) == 0
