@@ -146,8 +146,10 @@ FLCE_API flce_status flce_forward(const void* H, const void* W, const int64_t* l
  *                side unfiltered, for pretraining).  Requires the unfiltered gradient: with
  *                filter_threshold > 0, FLCE_ERR_ARG.  Twice the dW and dH tensor work.
  *                Options combine.  Other bits: FLCE_ERR_ARG.
- *   dH           (device) bf16 [N, Hd] (written)
- *   dW           (device) bf16 [V, Hd] (written, every row)
+ *   dH           (device) bf16 [N, Hd] (written), or NULL: dH is not computed
+ *   dW           (device) bf16 [V, Hd] (written, every row), or NULL: dW is not computed
+ *                (a frozen head, or hidden states that need no gradient, skip a quarter of
+ *                the step).  dH and dW both NULL: FLCE_ERR_ARG.
  *   workspace    (device) >= flce_backward_workspace_size(N, Hd, V, chunk_budget_bytes)
  *   chunk_budget_bytes  as passed to the size query (0 = default)
  * Cites: ai-infra-kb M011, §06 (recompute the logit tile, p = exp(z - lse),
@@ -219,6 +221,7 @@ FLCE_API flce_status flce_forward_noalloc(const void* H, const void* W, const in
  *   3. flce_backward_shard with the global lse and counts: dW_shard (bf16 [V_shard, Hd],
  *      complete) and dH_partial (fp32 [N, Hd], this shard's sum over its rows); the
  *      caller sums dH_partial over the shards (e.g. an all-reduce) and rounds as needed.
+ *      Either output may be NULL to skip it, as in flce_backward.
  *      A row whose label lives in another shard is still a valid row here.
  *      Workspace: flce_backward_workspace_size(N, Hd, V_shard, chunk_budget_bytes, options);
  *      FLCE_BWD_SORT_VOCAB sorts this shard's rows only.

@@ -196,8 +196,10 @@ def flce_forward(H, W, labels, ignore_index: int = -100, softcap: float = 0.0, r
 
 def flce_backward(H, W, labels, lse, counts, grad_out, ignore_index: int = -100, softcap: float = 0.0,
                   reduction="mean", chunk_budget: int = 0, workspace=None, dH=None, dW=None,
-                  filter_threshold: float = 0.0, sort_vocab: bool = False, compensated: bool = False):
-    """One backward call from the saved LSE and counts.  Returns (dH, dW) in bf16.
+                  filter_threshold: float = 0.0, sort_vocab: bool = False, compensated: bool = False,
+                  compute_dH: bool = True, compute_dW: bool = True):
+    """One backward call from the saved LSE and counts.  Returns (dH, dW) in bf16; a
+    gradient with compute_dH / compute_dW False is not computed and returned as None.
     filter_threshold > 0 turns on gradient filtering (softmax entries below it, other
     than the target, are dropped and all-zero blocks are skipped): an approximation.
     sort_vocab walks the vocabulary in mean-logit order (see vocab_order), which gathers
@@ -213,8 +215,10 @@ def flce_backward(H, W, labels, lse, counts, grad_out, ignore_index: int = -100,
     if g.numel() != (N if red == 2 else 1):
         raise FlceError("grad_out has %d elements" % g.numel())
     with torch.cuda.device(dev):
-        dH = dH if dH is not None else torch.empty_like(H)
-        dW = dW if dW is not None else torch.empty_like(W)
+        if not (compute_dH or compute_dW):
+            raise FlceError("nothing to compute: compute_dH and compute_dW are both False")
+        dH = None if not compute_dH else (dH if dH is not None else torch.empty_like(H))
+        dW = None if not compute_dW else (dW if dW is not None else torch.empty_like(W))
         need = backward_workspace_size(N, Hd, V, chunk_budget, sort_vocab, compensated)
         ws = workspace if workspace is not None else torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         _check(library().flce_backward(_p(H), _p(W), _p(labels), _p(lse), _p(counts), N, Hd, V, int(ignore_index),
@@ -313,10 +317,13 @@ class _FusedLinearCrossEntropy(torch.autograd.Function):
     def backward(ctx, grad):
         H, W, labels, lse, counts = ctx.saved_tensors
         ignore_index, softcap, reduction, chunk_budget, filter_threshold, sort_vocab, compensated = ctx.cfg
+        need_h, need_w = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        if not (need_h or need_w):
+            return (None,) * 10
         dH, dW = flce_backward(H, W, labels, lse, counts, grad, ignore_index, softcap, reduction, chunk_budget,
-                               filter_threshold=filter_threshold, sort_vocab=sort_vocab, compensated=compensated)
-        return (dH if ctx.needs_input_grad[0] else None, dW if ctx.needs_input_grad[1] else None,
-                None, None, None, None, None, None, None, None)
+                               filter_threshold=filter_threshold, sort_vocab=sort_vocab, compensated=compensated,
+                               compute_dH=need_h, compute_dW=need_w)
+        return (dH, dW, None, None, None, None, None, None, None, None)
 
 
 def linear_cross_entropy(hidden, weight, labels, ignore_index: int = -100, softcap: float = 0.0,

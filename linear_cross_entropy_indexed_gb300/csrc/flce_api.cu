@@ -444,9 +444,10 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
   BwdPlan pl;
   flce_status s = plan_backward(N, Hd, V, chunk_budget_bytes, options, &pl);
   if (s != FLCE_OK) return s;
-  if (!W || !dW || !counts) return FLCE_ERR_ARG;
-  if (N > 0 && (!H || !labels || !lse || !grad_out || (!dH && !dh_partial) || !workspace)) return FLCE_ERR_ARG;
-  if (!aligned(W, 16) || !aligned(dW, 16) || (H && !aligned(H, 16)) || (dH && !aligned(dH, 16)) ||
+  const bool want_dh = dH != nullptr || dh_partial != nullptr;  // either gradient may be skipped
+  if (!W || !counts || (!dW && !want_dh)) return FLCE_ERR_ARG;
+  if (N > 0 && (!H || !labels || !lse || !grad_out || !workspace)) return FLCE_ERR_ARG;
+  if (!aligned(W, 16) || (dW && !aligned(dW, 16)) || (H && !aligned(H, 16)) || (dH && !aligned(dH, 16)) ||
       (dh_partial && !aligned(dh_partial, 16)) ||
       !aligned(counts, 8) || (labels && !aligned(labels, 8)) || (lse && !aligned(lse, 4)) ||
       (grad_out && !aligned(grad_out, 4)))
@@ -458,7 +459,7 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (N == 0) {  // no tokens: the weight gradient is an empty sum
-    e = cudaMemsetAsync(dW, 0, size_t(V) * size_t(Hd) * 2, st);
+    e = dW ? cudaMemsetAsync(dW, 0, size_t(V) * size_t(Hd) * 2, st) : cudaSuccess;
     return e == cudaSuccess ? FLCE_OK : cuda_fail(e);
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -574,9 +575,11 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
       s5.k_blocks *= 2;
     }
     EpiDwParams p5{wc, v0, Hd, static_cast<__nv_bfloat16*>(dW), perm, V};
-    e = launch(FLCE_KERNEL_DW, st,
-               [&] { return launch_dw(tmDz_mn, tmLo_mn, tmH_mn, s5, p5, err, pair_grid(s5.units, sms), st); });
-    if (e != cudaSuccess) return cuda_fail(e);
+    if (dW) {
+      e = launch(FLCE_KERNEL_DW, st,
+                 [&] { return launch_dw(tmDz_mn, tmLo_mn, tmH_mn, s5, p5, err, pair_grid(s5.units, sms), st); });
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
 
     // dH (+)= dZ_chunk W_chunk
     Sched s6{};
@@ -599,9 +602,11 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
     EpiDhParams p6 = dh_partial != nullptr
                          ? EpiDhParams{N, Hd, dh_partial, nullptr, c == 0, 0}
                          : EpiDhParams{N, Hd, dh32, static_cast<__nv_bfloat16*>(dH), c == 0, c == pl.n_chunks - 1};
-    e = launch(FLCE_KERNEL_DH, st,
-               [&] { return launch_dh(tmDz_k, tmLo_k, tmW_mn, s6, p6, err, pair_grid(s6.units, sms), st); });
-    if (e != cudaSuccess) return cuda_fail(e);
+    if (want_dh) {
+      e = launch(FLCE_KERNEL_DH, st,
+                 [&] { return launch_dh(tmDz_k, tmLo_k, tmW_mn, s6, p6, err, pair_grid(s6.units, sms), st); });
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
   }
   return FLCE_OK;
 }
@@ -661,7 +666,6 @@ flce_status flce_backward(const void* H, const void* W, const int64_t* labels, c
                           int64_t N, int64_t Hd, int64_t V, int64_t ignore_index, float softcap, int reduction,
                           const float* grad_out, float filter_threshold, unsigned options, void* dH, void* dW,
                           void* workspace, size_t workspace_bytes, size_t chunk_budget_bytes, void* stream) {
-  if (N > 0 && !dH) return FLCE_ERR_ARG;
   return backward_impl(H, W, labels, lse, counts, N, Hd, V, 0, V, ignore_index, softcap, reduction, grad_out,
                        filter_threshold, options, dH, nullptr, dW, workspace, workspace_bytes, chunk_budget_bytes,
                        stream);
@@ -743,7 +747,6 @@ flce_status flce_backward_shard(const void* H, const void* W_shard, const int64_
                                 size_t chunk_budget_bytes, void* stream) {
   flce_status s = check_shard(V_shard, v_offset, V_total);
   if (s != FLCE_OK) return s;
-  if (N > 0 && !dH_partial) return FLCE_ERR_ARG;
   return backward_impl(H, W_shard, labels, lse, counts, N, Hd, V_shard, v_offset, V_total, ignore_index, softcap,
                        reduction, grad_out, filter_threshold, options, nullptr, dH_partial, dW_shard, workspace,
                        workspace_bytes, chunk_budget_bytes, stream);

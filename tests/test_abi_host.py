@@ -94,9 +94,9 @@ def _fwd(lib, H=0x1000, W=0x2000, labels=0x3000, N=16, Hd=64, V=100, red=0, loss
     return lib.flce_forward(H, W, labels, N, Hd, V, -100, softcap, red, loss, lse, None, counts, ws, ws_bytes, None)
 
 
-def _bwd(lib, N=16, Hd=64, V=100, red=0, filt=0.0, ws_bytes=1 << 24, dW=0x7000, W=0x2000, options=0):
+def _bwd(lib, N=16, Hd=64, V=100, red=0, filt=0.0, ws_bytes=1 << 24, dW=0x7000, W=0x2000, options=0, dH=0x9000):
     return lib.flce_backward(0x1000, W, 0x3000, 0x5000, 0x6000, N, Hd, V, -100, 0.0, red, 0x8000, filt, options,
-                             0x9000, dW, 0x10000, ws_bytes, 0, None)
+                             dH, dW, 0x10000, ws_bytes, 0, None)
 
 
 def test_argument_errors_before_any_device_work(lib):
@@ -114,7 +114,7 @@ def test_argument_errors_before_any_device_work(lib):
     assert _fwd(lib, N=1 << 40) == OVERFLOW
     assert _bwd(lib, filt=-0.5) == ARG
     assert _bwd(lib, filt=float("nan")) == ARG
-    assert _bwd(lib, dW=None) == ARG
+    assert _bwd(lib, dW=None, dH=None) == ARG   # nothing to compute
     assert _bwd(lib, ws_bytes=16) == WS
     assert _bwd(lib, W=0x2002) == ALIGN
     assert _bwd(lib, options=4) == ARG
