@@ -26,8 +26,8 @@
  *     elements).  labels is [N] int64.  Base addresses must be 16-byte aligned and
  *     Hd a multiple of 8 (TMA needs 16-byte row pitches).
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
- *     enqueued on it asynchronously; no call synchronises the host except on an
- *     argument error, which is detected before anything is enqueued.
+ *     enqueued on it asynchronously and no call synchronises the host; argument
+ *     errors are detected and returned before anything is enqueued.
  *   - A label equal to ignore_index is ignored.  A label outside [0, V) that is not
  *     ignore_index is "bad": it is counted in counts[1] and the row is treated as
  *     ignored (nothing traps on the device).
@@ -35,8 +35,9 @@
  *     the caller.  N == 0 is allowed (loss 0, counts 0, dW zeroed).
  *   - Results are deterministic: every reduction runs in a fixed order, so two calls
  *     on the same device with the same arguments give bitwise-identical outputs.
- *   - Device-side bounded waits that expire set bits in counts[2]
- *     (FLCE_DEVERR_*); the kernels then stop early instead of hanging.
+ *   - Device-side errors set bits in counts[2] (FLCE_DEVERR_*): a bounded wait that
+ *     expires (the kernels then stop early instead of hanging) or an out-of-range
+ *     vocabulary-order entry (the access is skipped).
  *   - Kernels are built for sm_103a only; other devices get FLCE_ERR_UNSUPPORTED.
  */
 #ifndef FLCE_H_
