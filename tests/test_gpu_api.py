@@ -49,24 +49,30 @@ def test_binding_rejects_bad_inputs():
         F.check_counts(counts)  # one label outside [0, V)
 
 
-def test_step_captured_in_a_cuda_graph():
+@pytest.mark.parametrize("mode", ["exact", "filtered_sorted", "compensated"])
+def test_step_captured_in_a_cuda_graph(mode):
     """Forward + backward through the C ABI captured once and replayed: the library
-    neither allocates nor synchronises, so the graph replays the same kernels."""
+    neither allocates nor synchronises, so the graph replays the same kernels (also with
+    the vocabulary order's sort and gather kernels, and with the compensated split)."""
     import linear_cross_entropy_indexed_gb300 as F
-    w = S.scaled("llama2", N=384, Hd=128, V=3000, seed=82, w_std=0.05)
+    opts = dict(exact={}, filtered_sorted=dict(filter_threshold=2.0 ** -12, sort_vocab=True),
+                compensated=dict(compensated=True))[mode]
+    w = S.scaled("unigram" if mode == "filtered_sorted" else "llama2", N=384, Hd=128, V=3000, seed=82, w_std=0.05)
     Hb, Wb, y = P.make_case(w)
     H, W = P.to_device(Hb), P.to_device(Wb)
     lab = torch.from_numpy(y).cuda()
     N, Hd, V = 384, 128, 3000
     budget = 384 * 2 * 1024
-    ws = torch.empty(max(F.forward_workspace_size(N, Hd, V), F.backward_workspace_size(N, Hd, V, budget)),
+    ws = torch.empty(max(F.forward_workspace_size(N, Hd, V),
+                         F.backward_workspace_size(N, Hd, V, budget, opts.get("sort_vocab", False),
+                                                   opts.get("compensated", False))),
                      dtype=torch.uint8, device="cuda")
     dH = torch.empty_like(H)
     dW = torch.empty_like(W)
     g = torch.ones(1, device="cuda")
     # eager reference and warm-up (device setup happens on the first call)
     loss_e, lse_e, counts_e, _ = F.flce_forward(H, W, lab, workspace=ws)
-    F.flce_backward(H, W, lab, lse_e, counts_e, g, chunk_budget=budget, workspace=ws, dH=dH, dW=dW)
+    F.flce_backward(H, W, lab, lse_e, counts_e, g, chunk_budget=budget, workspace=ws, dH=dH, dW=dW, **opts)
     torch.cuda.synchronize()
     dH_e, dW_e, loss_eager = dH.clone(), dW.clone(), loss_e.item()
     graph = torch.cuda.CUDAGraph()
@@ -75,7 +81,7 @@ def test_step_captured_in_a_cuda_graph():
     with torch.cuda.stream(stream):
         with torch.cuda.graph(graph, stream=stream):
             loss_g, lse_g, counts_g, _ = F.flce_forward(H, W, lab, workspace=ws)
-            F.flce_backward(H, W, lab, lse_g, counts_g, g, chunk_budget=budget, workspace=ws, dH=dH, dW=dW)
+            F.flce_backward(H, W, lab, lse_g, counts_g, g, chunk_budget=budget, workspace=ws, dH=dH, dW=dW, **opts)
     torch.cuda.current_stream().wait_stream(stream)
     dH.zero_()
     dW.zero_()
