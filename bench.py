@@ -294,6 +294,14 @@ def run_ours(args, w):
         c = per_class.setdefault(name, [0, 0.0])
         c[0] += 1
         c[1] += d
+    # per step: from the first launch's start event to the last launch's end event (every
+    # step launches the same kernels), reported as median and [0.2, 0.8] quantiles
+    L = launches // args.steps
+    step_ms = sorted(sink.start[k * L].elapsed_time(sink.end[(k + 1) * L - 1]) for k in range(args.steps))
+    q = lambda f: step_ms[min(len(step_ms) - 1, int(round(f * (len(step_ms) - 1))))]
+    fwd_classes = ("label_dot", "linear_lse", "lse_merge", "reduce")
+    fwd_ms = sum(v[1] for k, v in per_class.items() if k in fwd_classes) / args.steps
+    bwd_ms = sum(v[1] for k, v in per_class.items() if k not in fwd_classes) / args.steps
     # per step, summed over that class's launches; the compensated backward multiplies both
     # the bf16 value and the rounding remainder of dZ, twice the dW and dH products
     prod = 4.0 if args.compensated else 2.0
@@ -421,6 +429,8 @@ def run_ours(args, w):
             "workspace_mb": ws_bytes / 2**20,
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roof,
             "kernel_ms_per_step": {k: v[1] / args.steps for k, v in sorted(per_class.items())},
+            "step_ms": {"median": q(0.5), "q20": q(0.2), "q80": q(0.8),
+                        "forward_kernels": fwd_ms, "backward_kernels": bwd_ms},
         }
     if ws > 1:
         torch.distributed.barrier()
