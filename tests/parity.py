@@ -2,7 +2,8 @@
 C ABI (via the binding), and comparisons with the fp64 oracle.
 
 Tolerances (fp32 accumulation of bf16 products, bf16 gradient outputs):
-  loss      relative error <= 1e-3
+  loss      relative error <= 1e-3; where the exact loss is 0 with valid rows (V = 1),
+            absolute error <= (2e-3 + 1e-3) per reduced row; all rows ignored: exactly 0
   lse       absolute error <= 2e-3 per row
   target    absolute error <= 1e-3 per valid row (the indexed-dot output)
   dH, dW    relative Frobenius error <= 1e-2
@@ -84,8 +85,14 @@ def check_forward(out, ref: O.Forward, y, V, ignore_index=-100, reduction="mean"
     else:
         ref_l = float(ref.loss)
         got = float(out["loss"])
-        if ref_l == 0.0:
-            assert got == 0.0
+        if ref.n_valid == 0:
+            assert got == 0.0  # all rows ignored: zero by convention, exactly
+        elif ref_l == 0.0:
+            # every valid row's loss is exactly zero (V = 1: lse = z = target), so a relative
+            # error is undefined; bound it by the per-row lse and target tolerances summed
+            # over the rows the reduction adds up
+            rows = ref.n_valid if reduction == "sum" else 1
+            assert abs(got) <= rows * (TOL_LSE_ABS + TOL_TARGET_ABS), got
         else:
             assert abs(got - ref_l) / abs(ref_l) <= TOL_LOSS_REL, (got, ref_l)
     return dict(lse_err=float(lse_err), target_err=float(t_err))
