@@ -14,6 +14,7 @@ oracle on a bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import datetime
 import glob
 import hashlib
 import json
@@ -70,7 +71,7 @@ def load_peaks():
 
 # ---------------------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -100,28 +101,38 @@ class ClockSampler:
             self.fh.close()
         return False
 
-    def summary(self, sm_max_default=None):
+    def summary(self, sm_max_default=None, window=None):
+        """Median SM clock over the samples taken inside `window` (host wall-clock start
+        and end of the timed region; all samples if none falls inside), the highest max
+        clock, and every throttle reason seen in any sample."""
         out = {"sm_mhz": None, "sm_max_mhz": sm_max_default, "reasons": [], "samples": 0}
         if self.proc is None or not os.path.exists(self.path):
             out["reasons"] = ["clock sampling unavailable"]
             return out
-        sm, smax, reasons = [], [], set()
+        rows, reasons = [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                t = None
+            try:
+                rows.append((t, float(parts[2]), float(parts[3])))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            for n, v in zip(names, parts[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         os.unlink(self.path)
-        if sm:
-            out.update(sm_mhz=statistics.median(sm), sm_max_mhz=max(smax), samples=len(sm))
+        if rows:
+            inside = [r for r in rows if window and r[0] is not None and window[0] <= r[0] <= window[1]]
+            use = inside or rows
+            out.update(sm_mhz=statistics.median(r[1] for r in use), sm_max_mhz=max(r[2] for r in rows),
+                       samples=len(use), samples_all=len(rows),
+                       window="timed region" if inside else "all samples (none inside the timed region)")
         out["reasons"] = sorted(reasons)
         return out
 
@@ -269,12 +280,14 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        t_begin = time.time()
         with sink:
             e0.record(stream)
             for _ in range(args.steps):
                 loss, counts = step()
             e1.record(stream)
         torch.cuda.synchronize()
+        t_end = time.time()
         if ws > 1:
             torch.distributed.barrier()
     launches = F.launch_count() - n_launch0
@@ -286,7 +299,7 @@ def run_ours(args, w):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
     F.check_counts(counts)
-    clocks = clk.summary(peaks["sm_max"])
+    clocks = clk.summary(peaks["sm_max"], window=(t_begin, t_end))
 
     # per kernel class time inside the timed region (events on the launch stream)
     per_class = {}
@@ -465,7 +478,7 @@ def run_ours(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="llama3")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
