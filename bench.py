@@ -37,11 +37,12 @@ L2_BYTES = 129 * 10**6
 MEASURED_TRAFFIC = {
     # ncu capture of the four tensor-core kernels at the llama2 size (DRAM read + written
     # per launch), scaled by tiles per launch to llama3: x 4.008 for the linear-LSE launch
-    # (501 / 125 vocabulary tiles), x 2.004 for the per-chunk dZ / dW / dH launches
-    ("linear_lse", "llama3", "fa8d48f5b9b0d8fa"): 3.95e9,   # 0.981 + 0.005 GB at llama2
-    ("dz", "llama3", "fa8d48f5b9b0d8fa"): 4.64e9,           # 1.805 + 0.512 GB
-    ("dw", "llama3", "fa8d48f5b9b0d8fa"): 5.16e9,           # 2.316 + 0.257 GB
-    ("dh", "llama3", "fa8d48f5b9b0d8fa"): 5.15e9,           # 2.507 + 0.063 GB
+    # (501 / 125 vocabulary tiles), x 2.004 for the per-chunk dZ / dW / dH launches; both
+    # sizes have 32 token tiles, so the banded schedules stream W twice per launch in both
+    ("linear_lse", "llama3", "4349199516153f16"): 3.17e9,   # 0.786 + 0.005 GB at llama2
+    ("dz", "llama3", "4349199516153f16"): 2.37e9,           # 0.678 + 0.504 GB
+    ("dw", "llama3", "4349199516153f16"): 5.06e9,           # 2.270 + 0.256 GB
+    ("dh", "llama3", "4349199516153f16"): 5.02e9,           # 2.441 + 0.063 GB
 }
 
 

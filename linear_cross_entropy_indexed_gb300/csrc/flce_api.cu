@@ -36,6 +36,11 @@ constexpr size_t kAlign = 256;
 constexpr int kLseGroupMin = 4;  // vocabulary tiles per forward unit: range searched
 constexpr int kLseGroupMax = 8;
 constexpr int kPlanPairs = 76;   // SM pairs of a GB300 (152 SMs), for the planner
+// Token tiles per band of the M-first schedules (linear-LSE, dZ): 16 tiles of 256 rows
+// keep 16 x 256 x Hd x 2 bytes of H (32 MiB at Hd 4096) in L2 while W streams past
+// once per band, instead of H streaming past once per vocabulary tile when it does
+// not fit in L2 (N = 32768: 224 MiB).
+constexpr int kBandM = 16;
 constexpr size_t kDefaultChunkBudget = size_t(1) << 30;  // bf16 dZ chunk bytes
 constexpr int kMaxDevices = 64;
 
@@ -174,19 +179,34 @@ int64_t count_congruent(int64_t lo, int64_t hi, int64_t r, int64_t mod) {  // #{
   return upto(hi) - upto(lo);
 }
 
+// Makespan in tiles of the banded M-first unit order for G tiles per unit.  Every unit
+// has G tiles except those of the last group, which sit at the end of each band; with
+// more than kMaxBandsExact bands the tail is counted as if the order were unbanded
+// (the choice of G then hardly matters).
+constexpr int64_t kMaxBandsExact = 64;
+int64_t lse_makespan(int m_tiles, int v_tiles, int G, int band, int pairs) {
+  const int64_t ng = cdiv(v_tiles, G);
+  const int64_t units = int64_t(m_tiles) * ng;
+  const int64_t last = v_tiles - (ng - 1) * G;  // tiles in each unit of the last group
+  const int64_t bw = (band > 0 && band < m_tiles && cdiv(m_tiles, band) <= kMaxBandsExact) ? band : m_tiles;
+  int64_t t = 0;
+  for (int p = 0; p < pairs; ++p) {
+    int64_t tail = 0;
+    for (int64_t b0 = 0; b0 < m_tiles; b0 += bw) {  // the band of M-tiles [b0, b0 + w)
+      const int64_t w = std::min<int64_t>(bw, m_tiles - b0);
+      const int64_t start = b0 * ng + (ng - 1) * w;  // its last group's first unit
+      tail += count_congruent(start, start + w, p, pairs);
+    }
+    t = std::max(t, G * count_congruent(0, units, p, pairs) - (G - last) * tail);
+  }
+  return t;
+}
+
 int pick_lse_group(int m_tiles, int v_tiles, int pairs) {
   int best_g = kLseGroupMin;
   int64_t best_t = -1;
   for (int G = kLseGroupMin; G <= kLseGroupMax; ++G) {
-    const int64_t ng = cdiv(v_tiles, G);
-    const int64_t units = int64_t(m_tiles) * ng;
-    const int64_t last = v_tiles - (ng - 1) * G;  // tiles in each unit of the last group
-    int64_t t = 0;
-    for (int p = 0; p < pairs; ++p) {
-      const int64_t all = count_congruent(0, units, p, pairs);
-      const int64_t tail = count_congruent((ng - 1) * m_tiles, units, p, pairs);
-      t = std::max(t, G * all - (G - last) * tail);
-    }
+    const int64_t t = lse_makespan(m_tiles, v_tiles, G, kBandM, pairs);
     if (best_t < 0 || t <= best_t) {
       best_t = t;
       best_g = G;
@@ -407,6 +427,7 @@ flce_status forward_impl(const void* H, const void* W, const int64_t* labels, in
   sc.n_groups = pl.n_groups;
   sc.units = pl.m_tiles * pl.n_groups;
   sc.order = 0;
+  sc.band = kBandM;
   EpiLseParams lp{N, V, softcap, part_m, part_s};
   const int grid = pair_grid(sc.units, sms);
   e = launch(FLCE_KERNEL_LINEAR_LSE, st, [&] { return launch_linear_lse(tmH, tmW, sc, lp, err, grid, st); });
@@ -537,6 +558,7 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
     s4.n_groups = s4.n_tiles;
     s4.units = s4.m_tiles * s4.n_groups;
     s4.order = 0;
+    s4.band = kBandM;
     s4.b_n_off = static_cast<int>(w_off);
     if (filter && (e = cudaMemsetAsync(nz, 0, size_t(pl.nz_rows) * size_t(pl.nz_ld), st)) != cudaSuccess)
       return cuda_fail(e);

@@ -45,6 +45,10 @@ struct Sched {
   int n_groups;
   int units;
   int order;     // 0: consecutive units walk M first (share the B operand); 1: walk N first
+  // > 0: the dimension walked first is walked in bands of this many tiles: all units of
+  // one band (every tile of the other dimension) come before the next band's, so the
+  // band's operand tiles stay in L2 while the other operand streams past once per band.
+  int band;
   int b_n_off;   // added to the B operand's N coordinate (rows of W, K-major B)
   int b_k_off;   // added to the B operand's K coordinate (rows of W, MN-major B)
   // Block skipping over a filtered dZ chunk (null: off): per pair tile (M index), a

@@ -29,12 +29,28 @@
 namespace flce {
 
 __device__ __forceinline__ void decode_unit(const Sched& s, int u, int& mt, int& g) {
-  if (s.order == 0) {
-    g = u / s.m_tiles;
-    mt = u - g * s.m_tiles;
+  const int fast = s.order == 0 ? s.m_tiles : s.n_groups;  // dimension walked first
+  const int slow = s.order == 0 ? s.n_groups : s.m_tiles;
+  int f, sl;
+  if (s.band > 0 && s.band < fast) {
+    // band b holds fast-dimension tiles [b band, b band + width) crossed with every
+    // slow-dimension index; inside it the fast index varies first
+    const int per_band = s.band * slow;
+    const int b = u / per_band;
+    const int r = u - b * per_band;
+    const int width = min(s.band, fast - b * s.band);
+    sl = r / width;
+    f = b * s.band + (r - sl * width);
   } else {
-    mt = u / s.n_groups;
-    g = u - mt * s.n_groups;
+    sl = u / fast;
+    f = u - sl * fast;
+  }
+  if (s.order == 0) {
+    mt = f;
+    g = sl;
+  } else {
+    g = f;
+    mt = sl;
   }
 }
 
