@@ -224,7 +224,7 @@ flce_status plan_forward(int64_t N, int64_t Hd, int64_t V, int pairs, FwdPlan* p
   p->n_groups = cdiv(p->v_tiles, p->group);
   p->k_blocks = cdiv(Hd, kBK);
   p->dot_blocks = static_cast<int>(std::min<int64_t>(std::max<int64_t>(cdiv(N, kDotWarps), 1), kDotMaxBlocks));
-  p->merge_blocks = std::max(cdiv(N, kMergeThreads), 1);
+  p->merge_blocks = std::max(cdiv(N, kMergeRows), 1);
   size_t cur = 0, part;
   if (!mul_ok(size_t(p->n_groups) * kEpiSplit, size_t(N), &part) || !mul_ok(part, 4, &part))
     return FLCE_ERR_OVERFLOW;
@@ -436,7 +436,7 @@ flce_status forward_impl(const void* H, const void* W, const int64_t* labels, in
   // (3) fixed-order merge, per-row loss, block sums
   float* loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : nullptr;
   e = launch(FLCE_KERNEL_LSE_MERGE, st, [&] {
-    k_lse_merge<<<pl.merge_blocks, kMergeThreads, 0, st>>>(part_m, part_s, pl.n_groups * kEpiSplit, N, t_ws, labels,
+    k_lse_merge<<<pl.merge_blocks, kMergeRows * kMergeSlices, 0, st>>>(part_m, part_s, pl.n_groups * kEpiSplit, N, t_ws, labels,
                                                            ignore_index, V_total, lse, loss_rows, sums);
     return cudaGetLastError();
   });

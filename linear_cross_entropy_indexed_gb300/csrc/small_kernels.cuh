@@ -10,6 +10,8 @@ namespace flce {
 constexpr int kDotWarps = 8;        // rows per block of the indexed-dot kernel
 constexpr int kDotMaxBlocks = 2048; // grid cap (grid-stride beyond)
 constexpr int kMergeThreads = 256;
+constexpr int kMergeRows = 32;     // rows per block of the (m, s) merge: one per lane
+constexpr int kMergeSlices = 8;    // warps per merge block: each merges every 8th partial
 
 __device__ __forceinline__ float softcap_exact(float x, float c) {
   return c > 0.0f ? c * tanhf(x / c) : x;
@@ -83,25 +85,44 @@ __global__ void __launch_bounds__(32 * kDotWarps)
 }
 
 // Fixed-order merge of the per-group (max, sum) partials into lse_i, then the per-row
-// loss and a fixed-tree block sum (double) of the losses.
-__global__ void __launch_bounds__(kMergeThreads)
+// loss and a fixed-tree block sum (double) of the losses.  A block takes 32 rows, one
+// per lane, so every partial is read as one coalesced 128-byte line per warp; its 8 warps
+// split the partials (warp j merges groups j, j + 8, j + 16, ... in increasing order) so
+// that each row has 8 chains of loads in flight instead of one, and warp 0 then merges
+// the 8 slices in slice order.  The order of every merge is fixed: results are bitwise
+// reproducible.
+__device__ __forceinline__ void merge_ms(float& m, float& s, float mg, float sg) {
+  if (mg == -INFINITY) return;  // a group (or slice) that saw nothing
+  const float mn = fmaxf(m, mg);
+  s = s * exp2f(m - mn) + sg * exp2f(mg - mn);  // 2^-inf = 0 for the first merge
+  m = mn;
+}
+
+__global__ void __launch_bounds__(kMergeRows * kMergeSlices)
     k_lse_merge(const float* __restrict__ part_m, const float* __restrict__ part_s, int n_groups,
                 int64_t N, const float* __restrict__ t, const int64_t* __restrict__ labels,
                 int64_t ignore, int64_t V_total, float* __restrict__ lse_out, float* __restrict__ loss_rows,
                 double* __restrict__ blk_sums) {
-  __shared__ double sh[kMergeThreads];
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * kMergeThreads + threadIdx.x;
+  __shared__ float sm[kMergeSlices][kMergeRows], ss[kMergeSlices][kMergeRows];
+  const int lane = threadIdx.x & 31;
+  const int slice = threadIdx.x >> 5;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kMergeRows + lane;
+  float m = -INFINITY, s = 0.0f;
+  if (i < N) {
+#pragma unroll 4
+    for (int g = slice; g < n_groups; g += kMergeSlices)
+      merge_ms(m, s, part_m[static_cast<int64_t>(g) * N + i], part_s[static_cast<int64_t>(g) * N + i]);
+  }
+  sm[slice][lane] = m;
+  ss[slice][lane] = s;
+  __syncthreads();
+  if (slice != 0) return;
   double mine = 0.0;
   if (i < N) {
-    float m = -INFINITY, s = 0.0f;
-    for (int g = 0; g < n_groups; ++g) {
-      const float mg = part_m[static_cast<int64_t>(g) * N + i];
-      const float sg = part_s[static_cast<int64_t>(g) * N + i];
-      if (mg == -INFINITY) continue;  // a group that saw nothing
-      const float mn = fmaxf(m, mg);
-      s = s * exp2f(m - mn) + sg * exp2f(mg - mn);
-      m = mn;
-    }
+    m = -INFINITY;
+    s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kMergeSlices; ++k) merge_ms(m, s, sm[k][lane], ss[k][lane]);
     const float lse = (m + log2f(s)) * kLn2;
     lse_out[i] = lse;
     const int64_t y = labels[i];
@@ -110,13 +131,9 @@ __global__ void __launch_bounds__(kMergeThreads)
     if (loss_rows) loss_rows[i] = l;
     mine = l;
   }
-  sh[threadIdx.x] = mine;
-  __syncthreads();
-  for (int w = kMergeThreads / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) blk_sums[blockIdx.x] = sh[0];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mine += __shfl_down_sync(0xffffffffu, mine, off);
+  if (lane == 0) blk_sums[blockIdx.x] = mine;
 }
 
 // Single block: fixed-order totals of the block sums and block counts, then the
