@@ -87,8 +87,12 @@ FLCE_API size_t flce_forward_workspace_size(int64_t N, int64_t Hd, int64_t V);
 
 /* Bytes of scratch that flce_backward needs.  The backward walks the vocabulary in
    chunks of Vc columns and keeps one bf16 [N, Vc] dZ chunk plus an fp32 [N, Hd] dH
-   accumulator (the latter only when there is more than one chunk), plus one byte per
-   64 x 64 block of the chunk for the filtered mode.  With FLCE_BWD_SORT_VOCAB it also
+   accumulator (the latter only when there is more than one chunk, or when dH is split),
+   plus one byte per 64 x 64 block of the chunk for the filtered mode.  When the dH
+   product has too few 256 x 256 output tiles to fill the GPU's SM pairs evenly (fewer
+   than about 300: N x Hd below roughly 8192 x 4096), each tile's vocabulary range is
+   split into up to 4 parts and parts 2..4 keep their fp32 [N, Hd] sums here until they
+   are added to the accumulator.  With FLCE_BWD_SORT_VOCAB it also
    holds a bf16 [Vc, Hd] copy of the chunk's weight rows in sorted order and the order
    itself (about 28 bytes per vocabulary row); with FLCE_BWD_COMPENSATED a second bf16
    [N, Vc] chunk (the rounding remainder of dZ).
@@ -286,6 +290,7 @@ FLCE_API int flce_last_cuda_error(void);
 #define FLCE_KERNEL_VOCAB_KEYS 12  /* column mean of H, mean logit per vocabulary row     */
 #define FLCE_KERNEL_VOCAB_SORT 13  /* run sort + merge passes -> perm / inv               */
 #define FLCE_KERNEL_GATHER 14      /* sorted chunk's weight rows -> contiguous copy       */
+#define FLCE_KERNEL_DH_COMBINE 15  /* dH split: fp32 part sums added in part order        */
 FLCE_API uint64_t flce_launch_count(void);
 FLCE_API int flce_set_event_sink(void* const* start_events, void* const* end_events, int* kernel_ids,
                         int capacity);

@@ -257,13 +257,35 @@ bool plan_vocab(int64_t N, int64_t Hd, int64_t V, size_t* cur, VocabPlan* p) {
 struct BwdPlan {
   int64_t Vc = 0;
   int n_chunks = 0;
+  int dh_split = 1;            // K parts per dH output tile (1: no split)
   int nz_rows = 0, nz_ld = 0;  // token blocks x vocabulary blocks of the dZ block flags
   int dh_mask_ld = 0, dw_mask_ld = 0, mask_tok_tiles = 0, mask_voc_tiles = 0;
   bool sort = false, split = false;
   VocabPlan vocab;
-  size_t off_rows = 0, off_dz = 0, off_dz_lo = 0, off_dh = 0, off_nz = 0, off_dh_mask = 0, off_dw_mask = 0,
-         off_wperm = 0, total = 0;
+  size_t off_rows = 0, off_dz = 0, off_dz_lo = 0, off_dh = 0, off_dh_parts = 0, off_nz = 0, off_dh_mask = 0,
+         off_dw_mask = 0, off_wperm = 0, total = 0;
 };
+
+// K parts per dH output tile: the count (1 .. kMaxDhSplit, at most the chunk's K blocks)
+// whose units fill the launch's waves best, in waves of whole-K tiles.  A split costs
+// (parts - 1) fp32 [N, Hd] buffers and a pass that adds them, so it is taken only when it
+// shortens the launch by at least kMinDhSplitGain: 256 tiles on 76 pairs (4 waves ->
+// 3.5) split in 2, 128 tiles (2 -> 1.75) in 4, 512 tiles (7 -> 6.75) not at all.
+constexpr int kMaxDhSplit = 4;
+constexpr double kMinDhSplitGain = 0.05;
+int choose_dh_split(int64_t tiles, int pairs, int64_t k_blocks) {
+  const double whole = static_cast<double>(cdiv(tiles, pairs));
+  int best = 1;
+  double best_t = whole;
+  for (int S = 2; S <= kMaxDhSplit && S <= k_blocks; ++S) {
+    const double t = static_cast<double>(cdiv(tiles * S, pairs)) / S;
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = S;
+    }
+  }
+  return best_t <= (1.0 - kMinDhSplitGain) * whole ? best : 1;
+}
 
 // The chunk budget covers the bf16 dZ chunk (two of them, value and rounding remainder, in
 // the compensated mode) and, with the sorted vocabulary, the bf16 copy of the chunk's
@@ -283,18 +305,22 @@ flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, unsig
   if (vc > v_round) vc = v_round;
   p->Vc = vc;
   p->n_chunks = cdiv(V, vc);
+  // the compensated mode's two-part A operand is not split
+  p->dh_split = p->split ? 1 : choose_dh_split(int64_t(cdiv(N, kPairM)) * cdiv(Hd, kBN), kPlanPairs, cdiv(vc, kBK));
   p->nz_rows = cdiv(N, 64);
   p->nz_ld = static_cast<int>(vc / 64);
   p->dh_mask_ld = cdiv(p->nz_ld, 32);
   p->dw_mask_ld = cdiv(p->nz_rows, 32);
   p->mask_tok_tiles = cdiv(N, kPairM);
   p->mask_voc_tiles = static_cast<int>(vc / kPairM);
-  size_t cur = 0, dz, dh = 0;
+  size_t cur = 0, dz, dh = 0, parts = 0;
   if (!mul_ok(size_t(N), size_t(vc), &dz) || !mul_ok(dz, 2, &dz)) return FLCE_ERR_OVERFLOW;
-  if (p->n_chunks > 1 && (!mul_ok(size_t(N), size_t(Hd), &dh) || !mul_ok(dh, 4, &dh))) return FLCE_ERR_OVERFLOW;
+  if ((p->n_chunks > 1 || p->dh_split > 1) && (!mul_ok(size_t(N), size_t(Hd), &dh) || !mul_ok(dh, 4, &dh)))
+    return FLCE_ERR_OVERFLOW;
+  if (p->dh_split > 1 && !mul_ok(dh, size_t(p->dh_split - 1), &parts)) return FLCE_ERR_OVERFLOW;
   if (!reserve(&cur, size_t(N) * sizeof(RowInfo), &p->off_rows) || !reserve(&cur, dz, &p->off_dz) ||
-      !reserve(&cur, p->split ? dz : 0, &p->off_dz_lo) ||
-      !reserve(&cur, dh, &p->off_dh) || !reserve(&cur, size_t(p->nz_rows) * size_t(p->nz_ld), &p->off_nz) ||
+      !reserve(&cur, p->split ? dz : 0, &p->off_dz_lo) || !reserve(&cur, dh, &p->off_dh) ||
+      !reserve(&cur, parts, &p->off_dh_parts) || !reserve(&cur, size_t(p->nz_rows) * size_t(p->nz_ld), &p->off_nz) ||
       !reserve(&cur, size_t(p->mask_tok_tiles) * p->dh_mask_ld * 4, &p->off_dh_mask) ||
       !reserve(&cur, size_t(p->mask_voc_tiles) * p->dw_mask_ld * 4, &p->off_dw_mask))
     return FLCE_ERR_OVERFLOW;
@@ -487,7 +513,8 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
   RowInfo* rows = reinterpret_cast<RowInfo*>(ws + pl.off_rows);
   __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_dz);
   __nv_bfloat16* dz_lo = pl.split ? reinterpret_cast<__nv_bfloat16*>(ws + pl.off_dz_lo) : nullptr;
-  float* dh32 = pl.n_chunks > 1 ? reinterpret_cast<float*>(ws + pl.off_dh) : nullptr;
+  float* dh32 = (pl.n_chunks > 1 || pl.dh_split > 1) ? reinterpret_cast<float*>(ws + pl.off_dh) : nullptr;
+  float* dh_parts = pl.dh_split > 1 ? reinterpret_cast<float*>(ws + pl.off_dh_parts) : nullptr;
   uint8_t* nz = filter ? ws + pl.off_nz : nullptr;
   uint32_t* dh_mask = reinterpret_cast<uint32_t*>(ws + pl.off_dh_mask);
   uint32_t* dw_mask = reinterpret_cast<uint32_t*>(ws + pl.off_dw_mask);
@@ -621,13 +648,29 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
       s6.k_half = s6.k_blocks;
       s6.k_blocks *= 2;
     }
+    // K split of the exact product (the filtered mode keeps whole tiles for its K-step masks)
+    const int ksplit = filter ? 1 : std::min(pl.dh_split, s6.k_blocks);
+    s6.k_split = ksplit;
+    s6.units *= ksplit;
+    float* dh_acc = dh_partial != nullptr ? dh_partial : dh32;
+    const bool last = c == pl.n_chunks - 1;
     EpiDhParams p6 = dh_partial != nullptr
-                         ? EpiDhParams{N, Hd, dh_partial, nullptr, c == 0, 0}
-                         : EpiDhParams{N, Hd, dh32, static_cast<__nv_bfloat16*>(dH), c == 0, c == pl.n_chunks - 1};
+                         ? EpiDhParams{N, Hd, dh_partial, nullptr, c == 0, 0, dh_parts}
+                         : EpiDhParams{N, Hd, dh32, static_cast<__nv_bfloat16*>(dH), c == 0, last && ksplit == 1, dh_parts};
     if (want_dh) {
       e = launch(FLCE_KERNEL_DH, st,
                  [&] { return launch_dh(tmDz_k, tmLo_k, tmW_mn, s6, p6, err, pair_grid(s6.units, sms), st); });
       if (e != cudaSuccess) return cuda_fail(e);
+      if (ksplit > 1) {  // parts 1 .. ksplit - 1 into the running sum, or into the bf16 dH at the last chunk
+        __nv_bfloat16* out = (dh_partial == nullptr && last) ? static_cast<__nv_bfloat16*>(dH) : nullptr;
+        const int64_t count = N * Hd;
+        e = launch(FLCE_KERNEL_DH_COMBINE, st, [&] {
+          k_dh_combine<<<static_cast<int>(std::min<int64_t>(std::max<int64_t>(count / 4 / 256, 1), 8 * sms)), 256, 0,
+                         st>>>(dh_acc, dh_parts, ksplit - 1, count, out);
+          return cudaGetLastError();
+        });
+        if (e != cudaSuccess) return cuda_fail(e);
+      }
     }
   }
   return FLCE_OK;

@@ -56,6 +56,11 @@ struct Sched {
   // A K step whose slab is all zero is neither loaded nor multiplied.
   const uint32_t* kmask;
   int kmask_ld;
+  // K split (1: off; the exact dH product only): every output tile's K steps are split
+  // into k_split ranges run as separate units (units = k_split * m_tiles * n_groups, part
+  // index slowest); part ks covers K blocks [ks k_blocks / k_split, (ks + 1) k_blocks /
+  // k_split).  Fills the last wave of a launch that has few output tiles.
+  int k_split;
   // Two-part A operand (0: off): K steps [0, k_half) read A through the first tensor map,
   // steps [k_half, 2 k_half) the same coordinates through the second; B is read at the
   // step index modulo k_half, so the accumulator sums A1 B + A2 B.
@@ -105,6 +110,7 @@ struct EpiDhParams {
   float* acc32;         // [N, Hd] fp32 running sum across vocabulary chunks
   __nv_bfloat16* out;   // dH
   int first, last;
+  float* parts;         // K split: fp32 sums of K parts 1 .. k_split - 1, [k_split - 1][N][Hd]
 };
 
 // Launchers (defined in the kernel translation units).  Each returns the launch error.

@@ -136,6 +136,36 @@ __global__ void __launch_bounds__(kMergeRows * kMergeSlices)
   if (lane == 0) blk_sums[blockIdx.x] = mine;
 }
 
+// dH split: acc += parts[0] + parts[1] + ... in part order, 4 elements per thread per
+// step (16-byte loads; count = N Hd is a multiple of 8).  At the last vocabulary chunk
+// (out != null) the sum goes to the bf16 dH instead of back into the running sum.
+__global__ void __launch_bounds__(256)
+    k_dh_combine(float* __restrict__ acc, const float* __restrict__ parts, int n_parts, int64_t count,
+                 __nv_bfloat16* __restrict__ out) {
+  const int64_t n4 = count / 4;
+  for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < n4;
+       q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 v = reinterpret_cast<const float4*>(acc)[q];
+    for (int j = 0; j < n_parts; ++j) {
+      const float4 w = reinterpret_cast<const float4*>(parts + static_cast<int64_t>(j) * count)[q];
+      v.x += w.x;
+      v.y += w.y;
+      v.z += w.z;
+      v.w += w.w;
+    }
+    if (out != nullptr) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+      uint2 packed;
+      packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+      packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(out)[q] = packed;
+    } else {
+      reinterpret_cast<float4*>(acc)[q] = v;
+    }
+  }
+}
+
 // Single block: fixed-order totals of the block sums and block counts, then the
 // reduction (mean divides once by n_valid; 0 when n_valid == 0).
 __global__ void __launch_bounds__(256)

@@ -28,7 +28,13 @@
 
 namespace flce {
 
-__device__ __forceinline__ void decode_unit(const Sched& s, int u, int& mt, int& g) {
+__device__ __forceinline__ void decode_unit(const Sched& s, int u, int& mt, int& g, int& ks) {
+  ks = 0;
+  if (s.k_split > 1) {  // the K part is the slowest index
+    const int per_part = s.m_tiles * s.n_groups;
+    ks = u / per_part;
+    u -= ks * per_part;
+  }
   const int fast = s.order == 0 ? s.m_tiles : s.n_groups;  // dimension walked first
   const int slow = s.order == 0 ? s.n_groups : s.m_tiles;
   int f, sl;
@@ -128,7 +134,7 @@ struct EpiLse {
       st.m = mn;
     });
   }
-  __device__ static void tile(const Params& p, State& st, uint32_t taddr, int64_t, int nt, int h, uint8_t*) {
+  __device__ static void tile(const Params& p, State& st, uint32_t taddr, int64_t, int nt, int h, uint8_t*, int) {
     if (p.softcap > 0.0f)
       slices<true>(p, st, taddr, nt, h);
     else
@@ -229,7 +235,7 @@ struct EpiDz {
       }
     });
   }
-  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h, uint8_t*) {
+  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h, uint8_t*, int) {
     const bool cap = p.softcap > 0.0f;
     if (p.nz != nullptr) {  // filtering (the backward never combines it with the split)
       if (cap)
@@ -264,7 +270,8 @@ struct EpiDw {
   struct State {};
   __device__ static void unit_begin(const Params&, State&) {}
   __device__ static void unit_end(const Params&, State&, int64_t, int, int) {}
-  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h, uint8_t* stage) {
+  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h, uint8_t* stage,
+                                   int) {
     const int lane = threadIdx.x & 31;
     bool row_ok = row < p.rows_valid;
     int64_t orow = p.row0 + (row_ok ? row : 0);
@@ -302,12 +309,21 @@ struct EpiDw {
 // Backward: dH += dZ_chunk W_chunk; fp32 running sum across chunks, bf16 at the end.
 // The running sum's values for the next slice are loaded while the current one is
 // added, so the read-modify-write costs one memory latency per tile, not per slice.
+// With a K split, part 0 updates the running sum (never the bf16 output: the parts are
+// added afterwards) and part ks > 0 stores its fp32 sum into its own slice of `parts`.
 struct EpiDh {
   using Params = EpiDhParams;
   struct State {};
   __device__ static void unit_begin(const Params&, State&) {}
   __device__ static void unit_end(const Params&, State&, int64_t, int, int) {}
-  __device__ static void tile(const Params& p, State&, uint32_t taddr, int64_t row, int nt, int h, uint8_t* stage) {
+  __device__ static void tile(const Params& pp, State&, uint32_t taddr, int64_t row, int nt, int h, uint8_t* stage,
+                              int ks) {
+    Params p = pp;
+    if (ks > 0) {
+      p.acc32 = pp.parts + static_cast<int64_t>(ks - 1) * pp.N * pp.Hd;
+      p.first = 1;
+      p.last = 0;
+    }
     const int lane = threadIdx.x & 31;
     const int64_t mine = row < p.N ? row : -1;
     // step i moves rows 4i .. 4i+3 of the warp: lane -> row 4i + lane/8, 4-column chunk lane%8
@@ -433,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool leader = rank == 0;
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
+  const int ksplit = sched.k_split > 1 ? sched.k_split : 1;  // Sched{} leaves it 0: no split
   const uint32_t tiles_u32 = smem_u32(smem);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * kPairStages;
@@ -476,8 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t armed = 0, armed_parity = 0;
       bool ok = true;
       for (int u = pair; ok && u < sched.units; u += npairs) {
-        int mt, g;
-        decode_unit(sched, u, mt, g);
+        int mt, g, ks;
+        decode_unit(sched, u, mt, g, ks);
+        const int kb0 = ks * sched.k_blocks / ksplit;  // K split: this part's K blocks
+        const int kb1 = (ks + 1) * sched.k_blocks / ksplit;
         const int nt0 = g * sched.group;
         const int nt1 = min(nt0 + sched.group, sched.n_tiles);
         for (int nt = nt0; ok && nt < nt1; ++nt) {
@@ -501,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           };
           auto load_step = [&](int kb) -> bool { return load_k(&tmA, kb); };
           if (sched.kmask == nullptr && sched.k_half == 0) {
-            for (int kb = 0; kb < sched.k_blocks; ++kb)
+            for (int kb = kb0; kb < kb1; ++kb)
               if (!load_step(kb)) {
                 ok = false;
                 break;
@@ -538,8 +557,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true, issued = false;
       for (int u = pair; ok && u < sched.units; u += npairs) {
-        int mt, g;
-        decode_unit(sched, u, mt, g);
+        int mt, g, ks;
+        decode_unit(sched, u, mt, g, ks);
+        const int kb0 = ks * sched.k_blocks / ksplit;
+        const int kb1 = (ks + 1) * sched.k_blocks / ksplit;
         const int nt0 = g * sched.group;
         const int nt1 = min(nt0 + sched.group, sched.n_tiles);
         for (int nt = nt0; ok && nt < nt1; ++nt) {
@@ -550,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t d = tmem_base + acc * kBN;
           if (sched.kmask == nullptr) {
-            for (int kb = 0; kb < sched.k_blocks; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
               if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, err)) {
                 ok = false;
                 break;
@@ -560,7 +581,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t b = a + kATileBytes;
 #pragma unroll
               for (int k = 0; k < kBK / 16; ++k)
-                mma_bf16_pair(d, operand_desc<A_MN>(a, k), operand_desc<B_MN>(b, k), idesc, (kb | k) != 0 ? 1u : 0u);
+                mma_bf16_pair(d, operand_desc<A_MN>(a, k), operand_desc<B_MN>(b, k), idesc,
+                              ((kb - kb0) | k) != 0 ? 1u : 0u);
               issued = true;
               mma_commit_pair(empty0 + 8 * stage, 0x3);
               if (++stage == kPairStages) {
@@ -617,8 +639,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int u = pair; ok && u < sched.units; u += npairs) {
-      int mt, g;
-      decode_unit(sched, u, mt, g);
+      int mt, g, ks;
+      decode_unit(sched, u, mt, g, ks);
       const int nt0 = g * sched.group;
       const int nt1 = min(nt0 + sched.group, sched.n_tiles);
       const int64_t row = static_cast<int64_t>(mt) * (2 * kBM) + row_in_tile;
@@ -631,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
-        Epi::tile(ep, st, taddr, row, nt, h, epi_stage);
+        Epi::tile(ep, st, taddr, row, nt, h, epi_stage, ks);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(tempty0_lead + 8 * acc);

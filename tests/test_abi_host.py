@@ -68,8 +68,23 @@ def test_workspace_sizes(lib):
     flags = (n // 64) * (vc // 64)
     assert size >= n * vc * 2 + n * hd * 4 + n * 16 + flags
     assert size < n * vc * 2 + n * hd * 4 + n * 16 + flags + (1 << 12)
-    # a single chunk needs no fp32 accumulator
-    assert b(256, 64, 2000, 0, 0) < 256 * 2048 * 2 + 256 * 16 + 4096
+    # a single chunk needs no fp32 accumulator when dH is not split: 8192 x 4096 has 512 dH
+    # tiles of 256 x 256, which fill 76 SM pairs to within 4%, so it is not split
+    one = b(n, hd, 2000, 0, 0)
+    flags1 = (n // 64) * (2048 // 64)
+    assert n * 2048 * 2 + n * 16 + flags1 <= one < n * 2048 * 2 + n * 16 + flags1 + (1 << 12)
+    # few dH tiles: each tile's vocabulary range is split (256 x 64 is one tile: 4 parts),
+    # which needs the fp32 accumulator and three fp32 [N, Hd] part sums even for one chunk
+    small = b(256, 64, 2000, 0, 0)
+    base_s = 256 * 2048 * 2 + 256 * 16 + 4 * 256 * 64 * 4
+    assert base_s <= small < base_s + (256 // 64) * (2048 // 64) + (1 << 12)
+    # 4096 x 4096: 256 tiles, split in 2 (4 waves of 76 pairs -> 3.5): one part buffer
+    v2 = (budget // (2 * 4096)) // 256 * 256
+    two = b(4096, 4096, v, budget, 0)
+    base_2 = 4096 * v2 * 2 + 4096 * 16 + 2 * 4096 * 4096 * 4 + (4096 // 64) * (v2 // 64)
+    assert base_2 <= two < base_2 + (1 << 13)
+    # the compensated mode is never split
+    assert b(256, 64, 2000, 0, 2) < 2 * 256 * 2048 * 2 + 256 * 16 + (1 << 13)
     # the sorted vocabulary: the budget also covers the sorted bf16 weight rows of the
     # chunk, Vc = budget / (2N + 2Hd), plus the order (key, two sort words, perm, inv:
     # 28 bytes per vocabulary row) and the column sums of H

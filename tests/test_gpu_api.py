@@ -94,8 +94,9 @@ def test_step_captured_in_a_cuda_graph(mode):
 
 def test_skipping_a_gradient():
     """dW or dH can be skipped (NULL at the ABI): the other one is bit-identical to a full
-    backward and one kernel per vocabulary chunk is not launched; autograd asks for dH only
-    when the weight is frozen."""
+    backward and the skipped gradient's kernels are not launched (per vocabulary chunk the
+    dW product, or the dH product and, when dH is split, its combining pass); autograd asks
+    for dH only when the weight is frozen."""
     import linear_cross_entropy_indexed_gb300 as F
     w = S.scaled("llama3", N=300, Hd=128, V=3000, seed=61, w_std=0.05)
     Hb, Wb, y = P.make_case(w)
@@ -104,19 +105,22 @@ def test_skipping_a_gradient():
     loss, lse, counts, _ = F.flce_forward(H, W, lab)
     g = torch.ones(1, device="cuda")
     budget = 300 * 2 * 1024           # 3 vocabulary chunks
-    n0 = F.launch_count()
-    dH, dW = F.flce_backward(H, W, lab, lse, counts, g, chunk_budget=budget)
-    n_full = F.launch_count() - n0
-    n0 = F.launch_count()
-    dH_only, none_w = F.flce_backward(H, W, lab, lse, counts, g, chunk_budget=budget, compute_dW=False)
-    n_h = F.launch_count() - n0
-    n0 = F.launch_count()
-    none_h, dW_only = F.flce_backward(H, W, lab, lse, counts, g, chunk_budget=budget, compute_dH=False)
-    n_w = F.launch_count() - n0
-    torch.cuda.synchronize()
+
+    def run(**kw):
+        sink = F.EventSink(capacity=64)
+        with sink:
+            out = F.flce_backward(H, W, lab, lse, counts, g, chunk_budget=budget, **kw)
+        torch.cuda.synchronize()
+        return out, [name for name, _ in sink.durations_ms()]
+
+    (dH, dW), full = run()
+    (dH_only, none_w), h_only = run(compute_dW=False)
+    (none_h, dW_only), w_only = run(compute_dH=False)
     assert none_w is None and none_h is None
     assert torch.equal(dH_only, dH) and torch.equal(dW_only, dW)
-    assert n_h == n_full - 3 and n_w == n_full - 3
+    assert full.count("dw") == 3 and full.count("dh") == 3
+    assert h_only == [k for k in full if k != "dw"]
+    assert w_only == [k for k in full if k not in ("dh", "dh_combine")]
     with pytest.raises(F.FlceError, match="nothing to compute"):
         F.flce_backward(H, W, lab, lse, counts, g, compute_dH=False, compute_dW=False)
     # autograd with a frozen weight: H.grad matches, no dW launched
