@@ -39,10 +39,10 @@ MEASURED_TRAFFIC = {
     # per launch), scaled by tiles per launch to llama3: x 4.008 for the linear-LSE launch
     # (501 / 125 vocabulary tiles), x 2.004 for the per-chunk dZ / dW / dH launches; both
     # sizes have 32 token tiles, so the banded schedules stream W twice per launch in both
-    ("linear_lse", "llama3", "4349199516153f16"): 3.17e9,   # 0.786 + 0.005 GB at llama2
-    ("dz", "llama3", "4349199516153f16"): 2.37e9,           # 0.678 + 0.504 GB
-    ("dw", "llama3", "4349199516153f16"): 5.06e9,           # 2.270 + 0.256 GB
-    ("dh", "llama3", "4349199516153f16"): 5.02e9,           # 2.441 + 0.063 GB
+    ("linear_lse", "llama3", "226080fb59c1dd05"): 3.31e9,   # 0.822 + 0.004 GB at llama2
+    ("dz", "llama3", "226080fb59c1dd05"): 2.38e9,           # 0.683 + 0.505 GB
+    ("dw", "llama3", "226080fb59c1dd05"): 5.12e9,           # 2.300 + 0.257 GB
+    ("dh", "llama3", "226080fb59c1dd05"): 5.03e9,           # 2.446 + 0.063 GB
 }
 
 
