@@ -198,7 +198,12 @@ FLCE_API flce_status flce_vocab_order(const void* H, const void* W, int64_t N, i
  *     about 256K; larger problems must use flce_forward with their own workspace).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call before
- *     any stream capture.
+ *     any stream capture.  Under CUDA's lazy module loading that lookup may also load
+ *     the module on the device, reserving the 16 MiB and synchronising implicitly:
+ *     callers that cannot accept that on their hot path make the first call at
+ *     start-up.  A failed lookup is not remembered (the next call retries it) and
+ *     returns FLCE_ERR_CUDA with its error in flce_last_cuda_error(); an unsupported
+ *     device returns FLCE_ERR_UNSUPPORTED, as from flce_forward.
  *   - Every call shares the one array, which keeps the last call's contents.  Nothing
  *     in it has to start at zero: each call writes every scratch word before reading
  *     it.  Calls that overlap on the GPU (on two streams, or from two host threads)

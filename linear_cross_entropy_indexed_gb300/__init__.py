@@ -29,8 +29,8 @@ from . import _build
 __all__ = [
     "linear_cross_entropy", "FusedLinearCrossEntropyLoss", "flce_forward", "flce_backward", "flce_forward_shard", "flce_merge_shards",
     "flce_backward_shard", "forward_workspace_size",
-    "backward_workspace_size", "vocab_order", "FlceError", "check_counts", "library", "launch_count",
-    "EventSink", "KERNEL_NAMES",
+    "backward_workspace_size", "vocab_order", "FlceError", "check_counts", "check_pending", "library",
+    "launch_count", "EventSink", "KERNEL_NAMES",
 ]
 
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
@@ -292,16 +292,60 @@ def flce_backward_shard(H, W_shard, labels, lse, counts, grad_out, v_offset: int
     return dh, dw
 
 
+def _raise_on_counts(c, where: str = "", labels: bool = True) -> None:
+    if c[2] != 0:
+        raise FlceError("%sdevice error bits %#x (1: a bounded wait expired, 2: a vocabulary order index "
+                        "out of range)" % (where, c[2]))
+    if labels and c[1] != 0:
+        raise FlceError("%s%d labels outside [0, V) that are not ignore_index" % (where, c[1]))
+
+
 def check_counts(counts) -> tuple[int, int]:
     """Host check of a counts tensor (synchronises): raises on bad labels or on a
     device-side wait timeout; returns (n_valid, n_bad)."""
     c = counts.tolist()
-    if c[2] != 0:
-        raise FlceError("device error bits %#x (1: a bounded wait expired, 2: a vocabulary order index "
-                        "out of range)" % c[2])
-    if c[1] != 0:
-        raise FlceError("%d labels outside [0, V) that are not ignore_index" % c[1])
+    _raise_on_counts(c)
     return c[0], c[1]
+
+
+# Lazy checks of the autograd path.  After each forward and each backward of
+# linear_cross_entropy() the three counts are copied, on the launch stream, into pinned
+# host memory and an event is recorded; nothing waits.  The next call (or check_pending())
+# looks at every copy whose event has completed and raises FlceError if a forward saw
+# labels outside [0, V) (rows the kernels treated as ignored) or a forward or backward
+# set a device error bit.  The backward's copy reports error bits only, so a bad label
+# is reported once, by its forward.
+_pending = []
+_pending_lock = threading.Lock()
+
+
+def _watch_counts(counts, what: str, labels: bool) -> None:
+    if torch.cuda.is_current_stream_capturing():
+        return  # a captured graph has no host side to report to; use check_counts on its counts
+    host = torch.empty(3, dtype=torch.int64, pin_memory=True)
+    host.copy_(counts, non_blocking=True)
+    ev = torch.cuda.Event()
+    ev.record()
+    with _pending_lock:
+        _pending.append((ev, host, what, labels))
+
+
+def check_pending(wait: bool = False) -> int:
+    """Raise FlceError if an earlier linear_cross_entropy() forward saw labels outside
+    [0, V) that are not ignore_index, or a forward or backward set a device error bit.
+    Only copies whose event has completed are looked at, unless wait=True (which waits
+    for all of them).  Each step is reported once.  Returns how many are still pending."""
+    with _pending_lock:
+        done, left = [], []
+        for item in _pending:
+            if wait:
+                item[0].synchronize()
+            (done if item[0].query() else left).append(item)
+        _pending[:] = left
+        n_left = len(left)
+    for _, host, what, labels in done:
+        _raise_on_counts(host.tolist(), "an earlier %s: " % what, labels)
+    return n_left
 
 
 class _FusedLinearCrossEntropy(torch.autograd.Function):
@@ -309,6 +353,7 @@ class _FusedLinearCrossEntropy(torch.autograd.Function):
     def forward(ctx, H, W, labels, ignore_index, softcap, reduction, chunk_budget, filter_threshold, sort_vocab,
                 compensated):
         loss, lse, counts, _ = flce_forward(H, W, labels, ignore_index, softcap, reduction)
+        _watch_counts(counts, "linear_cross_entropy forward", labels=True)
         ctx.save_for_backward(H, W, labels, lse, counts)
         ctx.cfg = (ignore_index, softcap, reduction, chunk_budget, filter_threshold, sort_vocab, compensated)
         return loss
@@ -323,6 +368,7 @@ class _FusedLinearCrossEntropy(torch.autograd.Function):
         dH, dW = flce_backward(H, W, labels, lse, counts, grad, ignore_index, softcap, reduction, chunk_budget,
                                filter_threshold=filter_threshold, sort_vocab=sort_vocab, compensated=compensated,
                                compute_dH=need_h, compute_dW=need_w)
+        _watch_counts(counts, "linear_cross_entropy backward", labels=False)
         return (dH, dW, None, None, None, None, None, None, None, None)
 
 
@@ -334,7 +380,13 @@ def linear_cross_entropy(hidden, weight, labels, ignore_index: int = -100, softc
     int64.  reduction: "mean" (over rows whose label is valid), "sum" or "none".
     filter_threshold > 0 (e.g. 2**-12) makes the backward approximate, sort_vocab lets it
     skip more blocks, compensated makes the exact backward more precise: see
-    flce_backward."""
+    flce_backward.
+
+    Labels outside [0, V) that are not ignore_index are treated as ignored by the
+    kernels; they, and device error bits, are reported without a host synchronisation:
+    the next call (or check_pending()) raises FlceError once the step that saw them has
+    finished on the GPU."""
+    check_pending()
     Hd = hidden.shape[-1]
     H2 = hidden.reshape(-1, Hd)
     y = labels.reshape(-1)

@@ -338,6 +338,13 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 }  // namespace
 
+int check_device() {
+  int sms = 0;
+  return device_setup(&sms);
+}
+
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 // Sort keys (mean raw logit per vocabulary row), then the stable descending order:
 // perm[position] = row, inv[row] = position (inv may be null).
 flce_status vocab_order_impl(const void* H, const void* W, int64_t N, int64_t Hd, int64_t V, const VocabPlan& vp,

@@ -11,12 +11,16 @@
 // that loads this library holds that much memory until the process exits.  In host
 // code the array's name is only a host-side stand-in, so the device address is looked
 // up once per device with cudaGetSymbolAddress (with that device current) and passed
-// to the kernels like any workspace pointer.
+// to the kernels like any workspace pointer.  Under CUDA's lazy module loading the
+// lookup is also what loads the module on that device, so the first call per device
+// may reserve the 16 MiB and synchronise; callers that cannot accept that make their
+// first call at start-up.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "flce.h"
+#include "internal.cuh"
 
 namespace {
 
@@ -25,30 +29,29 @@ constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-struct ScratchAddress {
-  bool looked_up = false;
-  cudaError_t err = cudaSuccess;
-  void* ptr = nullptr;
-};
-ScratchAddress g_scratch[kMaxDevices];
+void* g_scratch[kMaxDevices] = {};  // device address per device, once looked up
 std::mutex g_scratch_mu;
 
-// Device address of the static scratch on the current device (looked up on the
-// first call per device).
+// Device address of the static scratch on the current device.  The device is checked
+// first (an unsupported GPU gets FLCE_ERR_UNSUPPORTED, as from flce_forward); only a
+// successful lookup is kept, so a failed one (say, made during a stream capture) is
+// retried by the next call, and its error is what flce_last_cuda_error() reports.
 flce_status static_scratch(void** out) {
+  const int st = flce::check_device();
+  if (st != FLCE_OK) return static_cast<flce_status>(st);
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FLCE_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return static_cast<flce_status>(flce::record_cuda_error(e));
   if (dev < 0 || dev >= kMaxDevices) return FLCE_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  ScratchAddress& s = g_scratch[dev];
-  if (!s.looked_up) {
+  if (g_scratch[dev] == nullptr) {
     void* p = nullptr;
-    s.err = cudaGetSymbolAddress(&p, g_static_scratch);
-    s.ptr = s.err == cudaSuccess ? p : nullptr;
-    s.looked_up = true;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return static_cast<flce_status>(flce::record_cuda_error(e));
+    if (p == nullptr) return static_cast<flce_status>(flce::record_cuda_error(cudaErrorInvalidSymbol));
+    g_scratch[dev] = p;
   }
-  if (s.err != cudaSuccess || s.ptr == nullptr) return FLCE_ERR_CUDA;
-  *out = s.ptr;
+  *out = g_scratch[dev];
   return FLCE_OK;
 }
 

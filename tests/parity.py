@@ -6,7 +6,15 @@ Tolerances (fp32 accumulation of bf16 products, bf16 gradient outputs):
             absolute error <= (2e-3 + 1e-3) per reduced row; all rows ignored: exactly 0
   lse       absolute error <= 2e-3 per row
   target    absolute error <= 1e-3 per valid row (the indexed-dot output)
-  dH, dW    relative Frobenius error <= 1e-2
+  dH, dW    relative Frobenius error <= 1e-2, and per row (a token row of dH, a
+            vocabulary row of dW) relative error <= 1e-2, a row's error measured against
+            max(its reference norm, 1e-3 x the largest reference row norm) so that rows
+            whose exact gradient is nearly zero are held to an absolute bound instead.
+            Derivation: each dZ entry is rounded to bf16 once (relative 2^-9) and each
+            output element once more (2^-9); a row whose terms all round the same way
+            is off by at most about 2 x 2^-9 = 3.9e-3 relative, fp32 accumulation adds
+            ~1e-6.  The per-row bound catches what the global norm hides: one wrong
+            256 x 256 output tile is 1/512 of an 8192 x 4096 dH but most of a row.
   counts    bit-exact
 """
 from __future__ import annotations
@@ -21,6 +29,8 @@ TOL_LOSS_REL = 1e-3
 TOL_LSE_ABS = 2e-3
 TOL_TARGET_ABS = 1e-3
 TOL_GRAD_FRO = 1e-2
+TOL_GRAD_ROW = 1e-2
+ROW_FLOOR = 1e-3
 
 
 def to_device(bits: np.ndarray, dev="cuda") -> torch.Tensor:
@@ -35,6 +45,30 @@ def fro_rel(a: np.ndarray, ref: np.ndarray) -> float:
     num = np.linalg.norm((a - ref).ravel())
     den = np.linalg.norm(ref.ravel())
     return float(num / den) if den > 0 else float(num)
+
+
+def row_rel_max(a: np.ndarray, ref: np.ndarray, floor_frac: float = ROW_FLOOR) -> float:
+    """Largest per-row error ||a_r - ref_r|| / max(||ref_r||, floor_frac * max_r ||ref_r||)
+    (absolute when every reference row is zero)."""
+    if a.size == 0:
+        return 0.0
+    num = np.linalg.norm(a - ref, axis=1)
+    den = np.linalg.norm(ref, axis=1)
+    top = den.max()
+    if top == 0:
+        return float(num.max())
+    return float((num / np.maximum(den, floor_frac * top)).max())
+
+
+def check_rows(name: str, got: np.ndarray, ref: np.ndarray, tol: float = TOL_GRAD_ROW) -> float:
+    e = row_rel_max(got, ref)
+    if e > tol:
+        num = np.linalg.norm(got - ref, axis=1)
+        den = np.maximum(np.linalg.norm(ref, axis=1), ROW_FLOOR * np.linalg.norm(ref, axis=1).max())
+        worst = np.argsort(-(num / den))[:5]
+        raise AssertionError("%s per-row rel err %g > %g (worst rows %s: %s)" % (
+            name, e, tol, worst.tolist(), (num / den)[worst].tolist()))
+    return e
 
 
 def make_case(w: S.Workload, labels: np.ndarray | None = None):
@@ -98,14 +132,20 @@ def check_forward(out, ref: O.Forward, y, V, ignore_index=-100, reduction="mean"
     return dict(lse_err=float(lse_err), target_err=float(t_err))
 
 
-def check_backward(out, dH_ref, dW_ref):
+def check_backward(out, dH_ref, dW_ref, no_grad_rows=None):
+    """Frobenius and per-row bounds on dH and dW; `no_grad_rows` (a boolean mask of
+    ignored or bad-label rows) must come out exactly zero in dH."""
     eh = fro_rel(out["dH"], dH_ref)
     ew = fro_rel(out["dW"], dW_ref)
     assert np.isfinite(out["dH"]).all() and np.isfinite(out["dW"]).all()
     assert eh <= TOL_GRAD_FRO, "dH rel fro err %g" % eh
     assert ew <= TOL_GRAD_FRO, "dW rel fro err %g" % ew
+    rh = check_rows("dH", out["dH"], dH_ref)
+    rw = check_rows("dW", out["dW"], dW_ref)
+    if no_grad_rows is not None and np.any(no_grad_rows):
+        assert np.all(out["dH"][np.asarray(no_grad_rows)] == 0.0), "an ignored row has a non-zero dH"
     assert int(out["counts_after"][2]) == 0, "device error bits set"
-    return dict(dH_err=eh, dW_err=ew)
+    return dict(dH_err=eh, dW_err=ew, dH_row_err=rh, dW_row_err=rw)
 
 
 def oracle_full(Hb, Wb, y, ignore_index=-100, softcap=0.0, reduction="mean", grad=None, filter_threshold=0.0):

@@ -172,3 +172,19 @@ def test_event_sink_toggles(lib):
     lib.flce_set_event_sink(None, None, None, 0)
     assert lib.flce_event_sink_used() == 0
     assert lib.flce_launch_count() >= 0
+
+
+def test_static_scratch_covers_the_documented_limit(lib):
+    """flce_forward_noalloc's static scratch holds the forward workspace of 8192 tokens
+    with a 256K vocabulary (the Gemma-2-shaped head) at every hidden size the workloads
+    use; the planner's vocabulary-tile group (at least 4 tiles per partial) is what keeps
+    it inside, so a planner change that breaks the documented limit fails here."""
+    import ctypes
+    lib.flce_static_scratch_bytes.restype = ctypes.c_size_t
+    limit = lib.flce_static_scratch_bytes()
+    assert limit == 16 << 20
+    for hd in (64, 2304, 3584, 4096, 8192):
+        need = lib.flce_forward_workspace_size(8192, hd, 256128)
+        assert 0 < need <= limit, (hd, need, limit)
+    assert lib.flce_forward_workspace_size(8192, 64, 1_000_000) > limit
+

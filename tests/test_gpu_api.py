@@ -1,5 +1,6 @@
-"""User-facing API on the GPU: the module form, argument checks of the binding, and a
-whole forward + backward step captured in a CUDA graph and replayed."""
+"""User-facing API on the GPU: the module form, argument checks of the binding, a
+whole forward + backward step captured in a CUDA graph and replayed, and the lazy,
+synchronisation-free report of bad labels in the autograd path."""
 import numpy as np
 import pytest
 import torch
@@ -129,3 +130,38 @@ def test_skipping_a_gradient():
     F.linear_cross_entropy(Hg, W, lab, chunk_budget=budget).backward()
     torch.cuda.synchronize()
     assert torch.equal(Hg.grad, dH) and W.grad is None
+
+
+def test_bad_label_is_reported_by_the_next_call():
+    """The autograd path does not synchronise to look at the counts: a label outside
+    [0, V) is treated as ignored by the kernels, and the next linear_cross_entropy() call
+    (here after the step has finished) raises FlceError; a clean step triggers no host
+    synchronisation and reports nothing."""
+    import linear_cross_entropy_indexed_gb300 as F
+    F.check_pending(wait=True)  # nothing left over from earlier tests
+    w = S.scaled("tiny", N=200, Hd=64, V=900, seed=83)
+    Hb, Wb, y = P.make_case(w)
+    H = P.to_device(Hb).requires_grad_(True)
+    W = P.to_device(Wb).requires_grad_(True)
+    good = torch.from_numpy(y).cuda()
+    bad = good.clone()
+    bad[5] = 900
+    torch.cuda.set_sync_debug_mode("error")  # any synchronising torch call raises
+    try:
+        F.linear_cross_entropy(H, W, good).backward()
+        loss = F.linear_cross_entropy(H, W, bad)   # nothing raised yet: nothing waited
+        loss.backward()
+    finally:
+        torch.cuda.set_sync_debug_mode("default")
+    torch.cuda.synchronize()
+    with pytest.raises(F.FlceError, match="1 labels outside"):
+        F.linear_cross_entropy(H, W, good)
+    # reported once: the following steps are clean
+    F.linear_cross_entropy(H, W, good).backward()
+    torch.cuda.synchronize()
+    assert F.check_pending(wait=True) == 0
+    # an explicit check after a bad step, without a further call
+    F.linear_cross_entropy(H, W, bad).backward()
+    with pytest.raises(F.FlceError, match="labels outside"):
+        F.check_pending(wait=True)
+    assert F.check_pending(wait=True) == 0

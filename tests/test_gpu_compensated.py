@@ -126,6 +126,9 @@ def test_full_size_llama3_compensated():
         e[False] + e[True] + floors))
     _check(dict(dH_err=e[False][0], dW_err=e[False][1]), dict(dH_err=e[True][0], dW_err=e[True][1]), floors)
     assert max(e[True]) <= P.TOL_GRAD_FRO
+    for c in got:
+        P.check_rows("dH", got[c][0], dh_ref)
+        P.check_rows("dW", got[c][1], dw_ref)
 
 
 def test_compensated_all_ignored_and_bad_labels():

@@ -76,5 +76,7 @@ def test_split_sharded_fp32_partial():
     dw = np.concatenate([S.bf16_bits_to_f32(P.bf16_bits(p[1])).astype(np.float64) for p in parts])
     ref, dH_ref, dW_ref = P.oracle_full(Hb, Wb, y)
     assert P.fro_rel(dh, dH_ref) <= P.TOL_GRAD_FRO and P.fro_rel(dw, dW_ref) <= P.TOL_GRAD_FRO
+    P.check_rows("dH", dh, dH_ref)
+    P.check_rows("dW", dw, dW_ref)
     # the fp32 partials are summed before any bf16 rounding: close to the oracle
     assert P.fro_rel(dh, dH_ref) <= 5e-3

@@ -8,11 +8,13 @@ Each case draws N, Hd and V from seeded lists that mix the tile boundaries (1, 1
 reduction, the softcap, a custom ignore_index, out-of-range labels, a vocabulary split
 into several backward chunks, and the backward options (exact, compensated, sorted
 vocabulary, gradient filtering with and without sorting).  Tolerances are those of
-the other parity tests (tests/parity.py); the filtered modes are compared with the
-oracle's filtered gradient."""
+the other parity tests (tests/parity.py), the per-row gradient bounds included, and
+ignored or bad-label rows must get an exactly zero dH row; the filtered modes are
+compared with the oracle's filtered gradient."""
 import numpy as np
 import pytest
 
+import oracle as O
 import synthetic as S
 from tests import parity as P
 
@@ -87,4 +89,5 @@ def test_shape_sweep(c):
                     compensated=c["mode"] == "compensated")
     ref, dH, dW = P.oracle_full(Hb, Wb, y, c["ignore_index"], c["softcap"], c["reduction"], filter_threshold=thr)
     P.check_forward(out, ref, y, c["V"], c["ignore_index"], c["reduction"])
-    P.check_backward(out, dH, dW)
+    valid, _ = O.label_status(y, c["V"], c["ignore_index"])
+    P.check_backward(out, dH, dW, no_grad_rows=~valid)

@@ -60,6 +60,8 @@ def test_three_ragged_shards_match_the_unsharded_oracle(softcap, reduction):
         assert abs(float(out["loss"]) - float(ref.loss)) <= P.TOL_LOSS_REL * abs(float(ref.loss))
     assert P.fro_rel(out["dH"], dH) <= P.TOL_GRAD_FRO
     assert P.fro_rel(out["dW"], dW) <= P.TOL_GRAD_FRO
+    P.check_rows("dH", out["dH"], dH)
+    P.check_rows("dW", out["dW"], dW)
 
 
 def test_chunked_shards_and_single_shard():
@@ -70,6 +72,8 @@ def test_chunked_shards_and_single_shard():
         out = _sharded(Hb, Wb, y, cuts=cuts, chunk_budget=budget)
         assert abs(float(out["loss"]) - float(ref.loss)) <= P.TOL_LOSS_REL * float(ref.loss)
         assert P.fro_rel(out["dH"], dH) <= P.TOL_GRAD_FRO and P.fro_rel(out["dW"], dW) <= P.TOL_GRAD_FRO
+        P.check_rows("dH", out["dH"], dH)
+        P.check_rows("dW", out["dW"], dW)
 
 
 def test_sharded_filtered_matches_filtered_oracle():
@@ -79,3 +83,5 @@ def test_sharded_filtered_matches_filtered_oracle():
     out = _sharded(Hb, Wb, y, cuts=(1200,), filter_threshold=thr)
     ref, dH, dW = P.oracle_full(Hb, Wb, y, filter_threshold=thr)
     assert P.fro_rel(out["dH"], dH) <= P.TOL_GRAD_FRO and P.fro_rel(out["dW"], dW) <= P.TOL_GRAD_FRO
+    P.check_rows("dH", out["dH"], dH)
+    P.check_rows("dW", out["dW"], dW)

@@ -2,7 +2,9 @@
 
 flce_vocab_order's keys are compared with the oracle's mean raw logits, and its
 permutation bit for bit with the oracle's order of the GPU's own fp32 keys (the float
-keys decide the integer order, so both sides take that decision on the same values).
+keys decide the integer order, so both sides take that decision on the same values);
+independently of the GPU keys, the oracle's keys taken in the permutation's order must
+not rise by more than the key tolerance.
 The sorted backward is compared element by element with the oracle's gradients, exact
 and filtered; it computes the same sums in another order.  Cases span several sort
 runs (4096 words each) and merge passes, ragged vocabulary chunks, the softcap and a
@@ -37,8 +39,15 @@ def _check_order(Hb, Wb, vocab=None):
     hbar = Hf.mean(axis=0) if Hf.shape[0] else np.zeros(Hf.shape[1])
     scale = np.linalg.norm(hbar) * np.linalg.norm(Wf[vs], axis=1) + np.abs(Wf[vs]).max(axis=1) * 1e-3
     err = np.abs(keys[vs].astype(np.float64) - ref)
-    assert np.all(err <= 2e-5 * scale + 1e-7), err.max()
+    tol = 2e-5 * scale + 1e-7
+    assert np.all(err <= tol), err.max()
     assert np.array_equal(perm, O.vocab_order(keys.astype(np.float64)))
+    if vocab is None:
+        # independently of the GPU keys: walked in perm order, the oracle's keys never rise
+        # by more than the two entries' key tolerances
+        rk, rt = ref[perm], tol[perm]
+        rise = rk[1:] - rk[:-1] - (rt[1:] + rt[:-1])
+        assert V < 2 or rise.max() <= 0.0, rise.max()
     assert np.array_equal(np.sort(perm), np.arange(V))
     assert np.array_equal(inv[perm], np.arange(V))
     return keys, perm
@@ -142,8 +151,10 @@ def test_sorted_vocab_shard():
     dh_ref = D @ Wf[off:off + vs]
     dw_ref = D.T @ Hf
     assert P.fro_rel(dh_part.double().cpu().numpy(), dh_ref) <= P.TOL_GRAD_FRO
+    P.check_rows("dH", dh_part.double().cpu().numpy(), dh_ref)
     got_w = S.bf16_bits_to_f32(P.bf16_bits(dw)).astype(np.float64)
     assert P.fro_rel(got_w, dw_ref) <= P.TOL_GRAD_FRO
+    P.check_rows("dW", got_w, dw_ref)
 
 
 def test_full_size_unigram_order_and_sorted_gradients():
@@ -178,6 +189,8 @@ def test_full_size_unigram_order_and_sorted_gradients():
         P.fro_rel(dh_got, dh_ref), P.fro_rel(dw_got, dw_ref)))
     assert P.fro_rel(dh_got, dh_ref) <= P.TOL_GRAD_FRO
     assert P.fro_rel(dw_got, dw_ref) <= P.TOL_GRAD_FRO
+    P.check_rows("dH", dh_got, dh_ref)
+    P.check_rows("dW", dw_got, dw_ref)
 
 
 def test_sorted_with_bad_labels_and_custom_ignore_index():

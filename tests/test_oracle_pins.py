@@ -6,7 +6,11 @@
 * central finite differences of the loss for dH and dW,
 * closed forms (W = 0, V = 1, huge logits, softcap -> infinity),
 * split invariance of the blockwise (m, s) merge over non-dividing chunk sizes,
-* label conventions (ignored rows, all ignored, out-of-range labels).
+* label conventions (ignored rows, all ignored, out-of-range labels),
+* the bf16 -> float64 widening every parity test feeds the oracle through, checked on
+  all 65536 bit patterns against a decoding of the format's sign, exponent and
+  fraction fields, and on values the format fixes (1.0, -3.0, the largest finite
+  value, the smallest subnormal 2^-133, the infinities).
 
 A final group plants mistakes in the oracle (monkeypatched, CPU only) and checks
 that at least one pin catches each of them.
@@ -309,11 +313,69 @@ def test_invariants():
     np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=1e-13)
 
 
+# ------------------------------------------------------------------ bf16 widening
+# The parity tests hand the oracle the same bf16 bit patterns the GPU reads; widen_bf16
+# turns them into float64.  bf16 is the upper half of an IEEE-754 binary32 value:
+# 1 sign bit, 8 exponent bits (bias 127), 7 stored fraction bits.
+INF = float("inf")
+BF16_FIXED = [  # (bits, value) fixed by that format
+    (0x0000, 0.0), (0x8000, -0.0), (0x3F80, 1.0), (0xBF80, -1.0), (0xC040, -3.0),
+    (0x3EAB, 0.333984375), (0x4049, 3.140625), (0x0001, 2.0 ** -133), (0x007F, 127 * 2.0 ** -133),
+    (0x0080, 2.0 ** -126), (0x7F7F, 3.3895313892515355e38), (0xFF7F, -3.3895313892515355e38),
+    (0x7F80, INF), (0xFF80, -INF),
+]
+
+
+def _bf16_from_fields(bits):
+    """Decode one 16-bit pattern from its sign, exponent and fraction fields."""
+    sign = -1.0 if bits >> 15 else 1.0
+    e = (bits >> 7) & 0xFF
+    f = bits & 0x7F
+    if e == 0xFF:
+        return sign * INF if f == 0 else float("nan")
+    if e == 0:                                   # subnormal: 0.f x 2^-126
+        return sign * math.ldexp(f, -126 - 7)
+    return sign * math.ldexp(128 + f, e - 127 - 7)  # normal: 1.f x 2^(e - 127)
+
+
+def pin_widen_bf16():
+    bits = np.array([b for b, _ in BF16_FIXED], dtype=np.uint16)
+    got = O.widen_bf16(bits)
+    assert got.dtype == np.float64
+    for (b, v), g in zip(BF16_FIXED, got):
+        assert g == v and math.copysign(1.0, g) == math.copysign(1.0, v), (hex(b), g, v)
+    with np.errstate(invalid="ignore"):        # signalling NaN patterns are among them
+        assert np.isnan(O.widen_bf16(np.array([0x7FC0, 0xFFC1, 0x7F81], dtype=np.uint16))).all()
+        # every one of the 65536 patterns against the field decoding
+        allb = np.arange(1 << 16, dtype=np.int64).astype(np.uint16)
+        w = O.widen_bf16(allb)
+    ref = np.array([_bf16_from_fields(b) for b in range(1 << 16)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(w), nan)
+    assert np.array_equal(w[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(w[~nan]), np.signbit(ref[~nan]))
+    # the value, not the byte order of the container, decides: a big-endian array widens alike
+    np.testing.assert_array_equal(O.widen_bf16(bits.astype(">u2")), got)
+    # shape is kept
+    with np.errstate(invalid="ignore"):
+        assert O.widen_bf16(allb.reshape(256, 256)).shape == (256, 256)
+    # binary32 values cut to their top 16 bits widen to exactly that truncated value
+    rng = np.random.default_rng(77)
+    x = (rng.standard_normal(4096) * np.exp(rng.uniform(-40.0, 40.0, 4096))).astype(np.float32)
+    u = x.view(np.uint32)
+    cut = (u & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)
+    np.testing.assert_array_equal(O.widen_bf16((u >> 16).astype(np.uint16)), cut)
+
+
+def test_widen_bf16():
+    pin_widen_bf16()
+
+
 # ------------------------------------------------------------------ planted mistakes
 ALL_PINS = [pin_worked_example, pin_two_tile_split, pin_torch_library,
             lambda: pin_torch_library(softcap=2.0), lambda: pin_torch_library(red="none"),
             pin_finite_differences, lambda: pin_finite_differences(softcap=1.5),
-            pin_closed_forms, pin_split_invariance, pin_label_conventions]
+            pin_closed_forms, pin_split_invariance, pin_label_conventions, pin_widen_bf16]
 
 
 def _caught():
@@ -360,16 +422,27 @@ def _mutants():
         y = np.asarray(labels)
         return y != ignore, np.zeros_like(y, dtype=bool)
 
+    def widen_shift8(bits):                    # bf16 placed 8 bits too low
+        return (np.asarray(bits).astype(np.uint32) << 8).view(np.float32).astype(np.float64)
+
+    def widen_byteswap(bits):                  # the two bytes of each value swapped
+        b = np.asarray(bits).astype(np.uint16).byteswap()
+        return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+    def widen_as_fp16(bits):                   # read as IEEE half precision instead of bf16
+        return np.asarray(bits).astype(np.uint16).view(np.float16).astype(np.float64)
+
     return [("_lse", lse_no_shift), ("_lse", lse_max_only), ("_cap_grad", cap_grad_one),
             ("_dlogits", dl_wrong_sign), ("_raw_logits", raw_reversed), ("row_scale", scale_by_rows),
-            ("merge", merge_no_rescale), ("label_status", status_no_range)]
+            ("merge", merge_no_rescale), ("label_status", status_no_range),
+            ("widen_bf16", widen_shift8), ("widen_bf16", widen_byteswap), ("widen_bf16", widen_as_fp16)]
 
 
 def test_pins_pass_on_the_oracle():
     assert _caught() == 0
 
 
-@pytest.mark.parametrize("mutant", range(8))
+@pytest.mark.parametrize("mutant", range(11))
 def test_planted_mistake_is_caught(mutant, monkeypatch):
     name, fn = _mutants()[mutant]
     monkeypatch.setattr(O, name, fn)

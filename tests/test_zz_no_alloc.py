@@ -37,7 +37,9 @@ def _p(t):
 
 
 @pytest.mark.parametrize("name,N,Hd,V,reduction", [("tiny", 300, 72, 1000, "mean"),
-                                                   ("gemma2", 520, 128, 3001, "none")])
+                                                   ("gemma2", 520, 128, 3001, "none"),
+                                                   # the documented limit: 8192 tokens, a 256K vocabulary
+                                                   ("gemma2", 8192, 64, 256128, "mean")])
 def test_noalloc_forward_matches_workspace_forward(name, N, Hd, V, reduction):
     F, lib = _lib()
     w = S.scaled(name, N=N, Hd=Hd, V=V, seed=31, w_std=0.1)
