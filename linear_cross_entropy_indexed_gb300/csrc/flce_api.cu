@@ -289,7 +289,9 @@ int choose_dh_split(int64_t tiles, int pairs, int64_t k_blocks) {
 
 // The chunk budget covers the bf16 dZ chunk (two of them, value and rounding remainder, in
 // the compensated mode) and, with the sorted vocabulary, the bf16 copy of the chunk's
-// weight rows in sorted order: Vc = budget / (2N (x2) (+ 2Hd)).
+// weight rows in sorted order: at most budget / (2N (x2) (+ 2Hd)) columns, a multiple of
+// 256.  The vocabulary is then cut into that many chunks of equal width (rounded up to
+// 256), so the last chunk is not a thin remainder with its own launch tails.
 flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, unsigned options, BwdPlan* p) {
   flce_status s = check_sizes(N, Hd, V);
   if (s != FLCE_OK) return s;
@@ -299,10 +301,11 @@ flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, unsig
   if (budget == 0) budget = kDefaultChunkBudget;
   const int64_t v_round = int64_t(cdiv(V, kBN)) * kBN;
   const size_t per_col = size_t(N) * (p->split ? 4 : 2) + (p->sort ? size_t(Hd) * 2 : 0);
-  int64_t vc = N > 0 ? static_cast<int64_t>(budget / per_col) : v_round;
-  vc = vc / kBN * kBN;
-  if (vc < kBN) vc = kBN;
-  if (vc > v_round) vc = v_round;
+  int64_t vc_max = N > 0 ? static_cast<int64_t>(std::min<size_t>(budget / per_col, size_t(v_round))) : v_round;
+  vc_max = vc_max / kBN * kBN;
+  if (vc_max < kBN) vc_max = kBN;
+  const int64_t want = cdiv(V, vc_max);                          // chunks the budget allows
+  const int64_t vc = int64_t(cdiv(cdiv(V, want), kBN)) * kBN;    // equal widths, <= vc_max
   p->Vc = vc;
   p->n_chunks = cdiv(V, vc);
   // the compensated mode's two-part A operand is not split

@@ -68,6 +68,11 @@ def test_workspace_sizes(lib):
     flags = (n // 64) * (vc // 64)
     assert size >= n * vc * 2 + n * hd * 4 + n * 16 + flags
     assert size < n * vc * 2 + n * hd * 4 + n * 16 + flags + (1 << 12)
+    # chunks of equal width: a 1 GiB budget allows 65536 columns, so V = 128256 takes two
+    # chunks, each ceil(128256 / 2) = 64128 columns rounded up to 256 = 64256
+    size_1g = b(n, hd, v, 1 << 30, 0)
+    base_1g = n * 64256 * 2 + n * hd * 4 + n * 16 + (n // 64) * (64256 // 64)
+    assert base_1g <= size_1g < base_1g + (1 << 14)  # + the K-step masks of the filtered mode
     # a single chunk needs no fp32 accumulator when dH is not split: 8192 x 4096 has 512 dH
     # tiles of 256 x 256, which fill 76 SM pairs to within 4%, so it is not split
     one = b(n, hd, 2000, 0, 0)
