@@ -7,9 +7,13 @@ Hd=4096, V=128256, bf16, Zipf(1.1) labels with 5% ignored, mean reduction.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config llama3] [--impl ours|reference]
 
-Under torchrun (N > 1) every rank runs its own batch (weak scaling, no collective in
-the data path); rank 0 prints one JSON line.  ``--impl reference`` times the fp64 CPU
-oracle on a bounded sample of the same workload instead.
+Under torchrun (N > 1) the step is token-sharded data parallel (weak scaling): every
+rank holds the same W and its own batch of N rows, and each step runs
+``dist.data_parallel_step`` — the local forward, an all-reduce of the valid counts and
+loss sums (the global mean divides once by the global valid count), the local backward
+scaled by that count, and an all-reduce of dW — with NCCL (``--dist-backend``).  Rank 0
+prints one JSON line with the collectives' share of the step.  ``--impl reference``
+times the fp64 CPU oracle on a bounded sample of the same workload instead.
 """
 from __future__ import annotations
 
@@ -165,10 +169,52 @@ def oracle_sample_step(Hf, Wf, y, w):
 
 
 def blas_threads() -> int:
+    """Threads numpy's BLAS actually uses: asked of the loaded OpenBLAS library itself,
+    else the usual environment variables, else the core count."""
+    import ctypes
+    try:
+        with open("/proc/self/maps") as fh:
+            libs = sorted({l.split()[-1] for l in fh if "openblas" in l.lower() and "/" in l})
+        for path in libs:
+            lib = ctypes.CDLL(path)
+            for name in ("openblas_get_num_threads", "openblas_get_num_threads64_",
+                         "scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads"):
+                if hasattr(lib, name):
+                    getattr(lib, name).restype = ctypes.c_int
+                    n = int(getattr(lib, name)())
+                    if n > 0:
+                        return n
+    except OSError:
+        pass
     for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         if os.environ.get(k):
             return int(os.environ[k])
     return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), with the online core count."""
+    name = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() == "Model name" and v.strip():
+                name = v.strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if name is None:
+        try:
+            with open("/proc/cpuinfo") as fh:
+                for line in fh:
+                    k, _, v = line.partition(":")
+                    if k.strip() in ("model name", "Model", "CPU part") and v.strip():
+                        name = v.strip()
+                        break
+        except OSError:
+            pass
+    return "%s, %d cores online" % (name or "unknown CPU", os.cpu_count() or 0)
 
 
 def cpu_baseline(w, sample_tokens: int, repeats: int = 1):
@@ -176,6 +222,7 @@ def cpu_baseline(w, sample_tokens: int, repeats: int = 1):
     workload: a full forward + backward of that smaller batch with the whole W."""
     import oracle as O
     import synthetic as S
+    sample_tokens = min(sample_tokens, w.N)  # the tiny workload is timed in full
     Hb = S.make_H(w, rows=slice(0, sample_tokens))
     y = S.make_labels(w)[:sample_tokens]
     Hf = O.widen_bf16(Hb)
@@ -186,7 +233,7 @@ def cpu_baseline(w, sample_tokens: int, repeats: int = 1):
         oracle_sample_step(Hf, Wf, y, w)
         times.append(time.perf_counter() - t0)
     t = statistics.median(times)
-    return dict(value=sample_tokens / t, unit="tokens/s", cores=blas_threads(), kind="oracle",
+    return dict(value=sample_tokens / t, unit="tokens/s", cores=blas_threads(), cpu_model=cpu_model(), kind="oracle",
                 sample="first %d of %d tokens of %s, full W [%d x %d]; fp64 forward + backward, %d run(s), "
                        "median %.2f s" % (sample_tokens, w.N, w.name, w.V, w.Hd, repeats, t),
                 seconds=t)
@@ -199,7 +246,7 @@ def run_reference(args, w):
         return 0
     import oracle as O
     import synthetic as S
-    n = args.ref_sample
+    n = min(args.ref_sample, w.N)
     Hf = O.widen_bf16(S.make_H(w, rows=slice(0, n)))
     y = S.make_labels(w)[:n]
     Wf = O.widen_bf16(S.make_W(w))
@@ -215,8 +262,8 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_desc(w), "sample_tokens_per_step": n},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-                         "sample": "first %d tokens of %s per step, full W" % (n, w.name)},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "cpu_model": cpu_model(),
+                         "kind": "oracle", "sample": "first %d tokens of %s per step, full W" % (n, w.name)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -232,16 +279,17 @@ def run_ours(args, w):
     ws, rank, local = dist_env()
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        torch.cuda.set_device(local % torch.cuda.device_count())
+        dist.init_process_group(args.dist_backend)
     else:
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
     peaks = load_peaks()
 
-    # inputs: each rank its own batch (seed offset by rank), resident in HBM
+    # inputs resident in HBM: the same W on every rank (replicated weights), each rank its
+    # own batch of H and labels (seed offset by rank)
     wr = S.scaled(w.name, seed=w.seed + 1000 * rank) if rank else w
-    Wb = S.make_W(wr)
+    Wb = S.make_W(w)
     Hb, yb = S.make_H(wr, W=Wb), S.make_labels(wr)
     to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(dev)
     H, W = to_dev(Hb), to_dev(Wb)
@@ -256,7 +304,35 @@ def run_ours(args, w):
     dW = torch.empty_like(W)
     g = torch.ones(1, dtype=torch.float32, device=dev)
 
+    # collectives of the data-parallel step, timed with events on the launch stream while
+    # `coll_on` holds (the timed region)
+    coll, coll_on = [], [False]
+
+    class CollTimer:
+        def __init__(self, name):
+            self.name = name
+
+        def __enter__(self):
+            if coll_on[0]:
+                self.e0 = torch.cuda.Event(enable_timing=True)
+                self.e0.record()
+            return self
+
+        def __exit__(self, *a):
+            if coll_on[0]:
+                e1 = torch.cuda.Event(enable_timing=True)
+                e1.record()
+                coll.append((self.name, self.e0, e1))
+            return False
+
     def step():
+        if ws > 1:
+            from linear_cross_entropy_indexed_gb300.dist import data_parallel_step
+            loss, _, _, counts = data_parallel_step(
+                H, W, y, g, w.ignore_index, w.softcap, timer=CollTimer, workspace=workspace, chunk_budget=budget,
+                dH=dH, dW=dW, filter_threshold=args.filter_threshold, sort_vocab=args.sort_vocab,
+                compensated=args.compensated)
+            return loss, counts
         loss, lse, counts, _ = F.flce_forward(H, W, y, w.ignore_index, w.softcap, red, workspace=workspace)
         F.flce_backward(H, W, y, lse, counts, g, w.ignore_index, w.softcap, red, budget, workspace=workspace,
                         dH=dH, dW=dW, filter_threshold=args.filter_threshold, sort_vocab=args.sort_vocab,
@@ -282,11 +358,13 @@ def run_ours(args, w):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         t_begin = time.time()
+        coll_on[0] = True
         with sink:
             e0.record(stream)
             for _ in range(args.steps):
                 loss, counts = step()
             e1.record(stream)
+        coll_on[0] = False
         torch.cuda.synchronize()
         t_end = time.time()
         if ws > 1:
@@ -301,6 +379,17 @@ def run_ours(args, w):
         ms = float(t.item())
     F.check_counts(counts)
     clocks = clk.summary(peaks["sm_max"], window=(t_begin, t_end))
+
+    # the data-parallel collectives' time per step (events on the launch stream around each)
+    coll_summary = None
+    if ws > 1:
+        per = {}
+        for name, a, b in coll:
+            per[name] = per.get(name, 0.0) + a.elapsed_time(b)
+        tot = sum(per.values()) / args.steps
+        coll_summary = {"ms_per_step": {k: v / args.steps for k, v in sorted(per.items())},
+                        "share_of_step": tot / ms, "backend": args.dist_backend,
+                        "what": "all-reduce of counts and per-rank loss sums (global mean), all-reduce of dW"}
 
     # per kernel class time inside the timed region (events on the launch stream)
     per_class = {}
@@ -372,11 +461,17 @@ def run_ours(args, w):
             b = bufs[i % 2]
             cur = torch.cuda.current_stream(dev)
             cur.wait_event(copied[i % 2])
-            Hx = b[0].detach().requires_grad_(True)
-            Wx = b[1].detach().requires_grad_(True)
-            loss = F.linear_cross_entropy(Hx, Wx, b[2], w.ignore_index, w.softcap, red, budget, args.filter_threshold,
-                                          args.sort_vocab, args.compensated)
-            loss.backward()
+            if ws > 1:  # the public data-parallel step: exchange of counts and loss, dW all-reduce
+                from linear_cross_entropy_indexed_gb300.dist import data_parallel_step
+                loss, _, _, _ = data_parallel_step(
+                    b[0], b[1], b[2], g, w.ignore_index, w.softcap, chunk_budget=budget,
+                    filter_threshold=args.filter_threshold, sort_vocab=args.sort_vocab, compensated=args.compensated)
+            else:
+                Hx = b[0].detach().requires_grad_(True)
+                Wx = b[1].detach().requires_grad_(True)
+                loss = F.linear_cross_entropy(Hx, Wx, b[2], w.ignore_index, w.softcap, red, budget,
+                                              args.filter_threshold, args.sort_vocab, args.compensated)
+                loss.backward()
             freed[i % 2].record(cur)
             loss_host[i % 2].copy_(loss.detach().reshape(1), non_blocking=True)
             loss_ready[i % 2].record(cur)
@@ -421,7 +516,9 @@ def run_ours(args, w):
         bi = Hh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 8
         e2e = {"value": ws * N / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": 4, "ms_per_step": e2e_ms, "steps": k2, "h2d_ms_per_step": h2d_ms,
-               "path": "linear_cross_entropy() autograd; pinned H, W, labels copied every step on a copy "
+               "path": ("dist.data_parallel_step() (NCCL exchange of counts and loss, dW all-reduce)" if ws > 1 else
+                        "linear_cross_entropy() autograd") +
+                       "; pinned H, W, labels copied every step on a copy "
                        "stream (next step's copy overlaps this step's compute); every step's loss copied to pinned host "
                        "memory and read on the host once the next step is enqueued"}
 
@@ -463,6 +560,7 @@ def run_ours(args, w):
             "workspace_mb": ws_bytes / 2**20,
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roof,
             "kernel_ms_per_step": {k: v[1] / args.steps for k, v in sorted(per_class.items())},
+            "collectives": coll_summary,
             "step_ms": {"median": q(0.5), "q20": q(0.2), "q80": q(0.8),
                         "forward_kernels": fwd_ms, "backward_kernels": bwd_ms},
         }
@@ -496,6 +594,8 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=1024)
     ap.add_argument("--ref-sample", type=int, default=64)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--dist-backend", default="nccl", choices=["nccl", "gloo"],
+                    help="process-group backend of the data-parallel exchange when N > 1 (gloo: host copies)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

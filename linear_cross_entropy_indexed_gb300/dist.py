@@ -11,7 +11,7 @@ summed by the ordinary data-parallel gradient all-reduce.
 Nothing here runs arithmetic of the loss itself; the collectives go through
 torch.distributed (NCCL for device tensors, gloo for CPU tensors).
 
-Recipe per step::
+Recipe per step (``data_parallel_step`` runs it)::
 
     loss_sum, lse, counts, _ = flce_forward(H_r, W, y_r, reduction="sum")
     allreduce_counts_(counts)                    # counts[0] = global valid count
@@ -51,3 +51,47 @@ def global_mean_loss(local_loss_sum: torch.Tensor, counts_global: torch.Tensor, 
     dist.all_reduce(total, op=dist.ReduceOp.SUM, group=group)
     n = counts_global[0].to(torch.float64)
     return torch.where(n > 0, total[0] / torch.clamp(n, min=1), torch.zeros_like(total[0])).to(torch.float32)
+
+
+def data_parallel_step(H, W, labels, grad_out=1.0, ignore_index: int = -100, softcap: float = 0.0, group=None,
+                       forward=None, backward=None, reduce_dW: bool = True, timer=None, **backward_kw):
+    """One token-sharded forward + backward of this rank's rows (the recipe above).
+
+    Returns (loss, dH, dW, counts): the global mean loss (every rank gets the same
+    value), this rank's rows of dH, dW summed over the ranks (this rank's part only when
+    reduce_dW is False, for callers whose optimizer reduces gradients itself), and the
+    exchanged counts [global valid, global bad, error bits of any rank] for check_counts.
+    ``forward`` / ``backward`` default to the library's flce_forward / flce_backward and
+    take their arguments.  ``timer``, if given, is a context-manager factory wrapped
+    around each collective (the benchmark times them with CUDA events)."""
+    if forward is None or backward is None:
+        from . import flce_backward, flce_forward
+        forward = forward or flce_forward
+        backward = backward or flce_backward
+    timer = timer or _no_timer
+    workspace = backward_kw.pop("workspace", None)
+    loss_sum, lse, counts, _ = forward(H, W, labels, ignore_index, softcap, "sum", workspace=workspace)
+    with timer("counts"):
+        allreduce_counts_(counts, group)
+        loss = global_mean_loss(loss_sum, counts, group)
+    g = grad_out if torch.is_tensor(grad_out) else torch.tensor([float(grad_out)], dtype=torch.float32,
+                                                                 device=counts.device)
+    dH, dW = backward(H, W, labels, lse, counts, g, ignore_index, softcap, "mean", workspace=workspace,
+                      **backward_kw)
+    if reduce_dW and dW is not None:
+        with timer("dW"):
+            dist.all_reduce(dW, op=dist.ReduceOp.SUM, group=group)
+    return loss, dH, dW, counts
+
+
+class _NoTimer:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def _no_timer(name):
+    return _NoTimer()
+

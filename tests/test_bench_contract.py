@@ -41,6 +41,7 @@ def test_reference_arm_line():
     assert d["impl"] == "reference" and d["dtype"] == "f64"
     c = d["cpu_baseline"]
     assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] == d["value"] and "sample" in c
+    assert "cores online" in c["cpu_model"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
 
 
@@ -65,4 +66,34 @@ def test_our_arm_line():
     assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] == 4
     c = d["cpu_baseline"]
     assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0 and "sample" in c
+    assert "cores online" in c["cpu_model"]
     assert d["peak_extra_mb"] >= 0
+
+
+@pytest.mark.gpu
+def test_two_rank_data_parallel_line():
+    """bench.py's N > 1 path (dist.data_parallel_step with its exchange and dW all-reduce),
+    launched the way the driver launches it, with two ranks on the one GPU of this machine.
+    The exchange goes through gloo (host copies): NCCL wants one GPU per rank.  The
+    kernels of the two ranks never wait on each other; only the host-side collectives
+    do.  This checks the code path and the JSON line, not multi-GPU performance."""
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--gpus", "2", "--steps", "3", "--warmup", "3", "--config", "tiny", "--dist-backend", "gloo",
+           "--no-cpu-baseline"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.strip().splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    d = json.loads(lines[0])
+    for k in COMMON:
+        assert k in d, k
+    assert d["n_gpus"] == 2 and d["scaling"] == "weak" and d["config"]["global_batch"] == 2 * 256
+    c = d["collectives"]
+    assert set(c["ms_per_step"]) == {"counts", "dW"} and 0 < c["share_of_step"] < 1
+    assert d["e2e"]["value"] > 0 and "data_parallel_step" in d["e2e"]["path"]

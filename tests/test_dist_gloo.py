@@ -3,7 +3,9 @@
 Token-sharded data parallel: each rank runs the fp64 oracle on its rows as its local
 step, the ranks exchange (loss sum, valid count) with the helpers of
 ``linear_cross_entropy_indexed_gb300.dist`` and all-reduce dW; the result must equal
-the unsharded oracle.  Vocab-parallel: each rank holds a vocabulary shard, computes
+the unsharded oracle.  The same holds for ``dist.data_parallel_step`` (the step
+bench.py times with NCCL on N > 1 GPUs) with the oracle passed in as its forward and
+backward.  Vocab-parallel: each rank holds a vocabulary shard, computes
 per-row (max, sum, target) over it, and the ranks merge them in rank order with the
 running (m, s) rule (ai-infra-kb M011 §05 and §07); the merged LSE and loss must equal
 the unsharded oracle."""
@@ -54,6 +56,52 @@ def _dp_worker(rank, world, port, q, all_ignored_rank1):
         dWt = torch.from_numpy(dW)
         dist.all_reduce(dWt)
         q.put((rank, float(loss), int(counts[0]), sl.start, sl.stop, dH, dWt.numpy()))
+    finally:
+        dist.destroy_process_group()
+
+
+def _oracle_forward(H, W, labels, ignore_index, softcap, reduction, workspace=None):
+    """The fp64 oracle in the shape of flce_forward's return value (CPU tensors)."""
+    import oracle as O
+    f = O.forward(H.numpy(), W.numpy(), labels.numpy(), ignore_index, softcap, reduction)
+    counts = torch.tensor([f.n_valid, f.n_bad, 0], dtype=torch.int64)
+    return torch.tensor(float(f.loss), dtype=torch.float64), torch.from_numpy(f.lse), counts, None
+
+
+def _oracle_backward(H, W, labels, lse, counts, grad_out, ignore_index, softcap, reduction, workspace=None):
+    """The fp64 oracle in the shape of flce_backward: like the library, the mean scale is
+    grad / counts[0] with whatever count counts holds (the global one after the exchange)."""
+    import oracle as O
+    assert reduction == "mean"
+    n = int(counts[0])
+    g = float(grad_out.reshape(-1)[0]) / n if n else 0.0
+    dH, dW = O.backward(H.numpy(), W.numpy(), labels.numpy(), lse.numpy(), ignore_index, softcap, "sum", g)
+    return torch.from_numpy(dH), torch.from_numpy(dW)
+
+
+def _dp_step_worker(rank, world, port, q, all_ignored_rank1):
+    from linear_cross_entropy_indexed_gb300.dist import data_parallel_step, shard_rows
+    dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % port, rank=rank, world_size=world)
+    try:
+        H, W, y = _data(all_ignored_rank1=all_ignored_rank1)
+        sl = shard_rows(len(y), world, rank)
+        names = []
+
+        class Timer:
+            def __init__(self, name):
+                names.append(name)
+
+            def __enter__(self):
+                return self
+
+            def __exit__(self, *a):
+                return False
+
+        loss, dH, dW, counts = data_parallel_step(torch.from_numpy(H[sl]), torch.from_numpy(W), torch.from_numpy(y[sl]),
+                                          grad_out=torch.tensor([1.3], dtype=torch.float64), softcap=0.0,
+                                          forward=_oracle_forward, backward=_oracle_backward, timer=Timer)
+        assert counts.tolist() == [int((y != -100).sum()), 0, 0]
+        q.put((rank, float(loss), sl.start, sl.stop, dH.numpy(), dW.numpy(), names))
     finally:
         dist.destroy_process_group()
 
@@ -137,3 +185,21 @@ def test_vocab_parallel_merge_matches_unsharded():
         Zr = H @ W[:W.shape[0] // 2].T
         own = Zr.max(1) + np.log(np.exp(Zr - Zr.max(1)[:, None]).sum(1))
         assert np.abs(own - ref.lse).max() > 0.1
+
+
+@pytest.mark.parametrize("all_ignored_rank1", [False, True])
+def test_data_parallel_step_matches_unsharded(all_ignored_rank1):
+    """dist.data_parallel_step, the step bench.py times on N > 1 GPUs, with the fp64
+    oracle standing in for the CUDA forward / backward: loss, every rank's dH rows and
+    the all-reduced dW equal the unsharded oracle, also when one rank has no valid row."""
+    import oracle as O
+    res = _run(_dp_step_worker, all_ignored_rank1)
+    H, W, y = _data(all_ignored_rank1=all_ignored_rank1)
+    ref = O.forward(H, W, y)
+    dH_ref, dW_ref = O.backward(H, W, y, ref.lse, grad_out=1.3)
+    for rank, loss, a, b, dH, dW, names in res:
+        assert abs(loss - float(ref.loss)) <= 1e-6 * abs(float(ref.loss))
+        np.testing.assert_allclose(dH, dH_ref[a:b], rtol=1e-10, atol=1e-14)
+        np.testing.assert_allclose(dW, dW_ref, rtol=1e-10, atol=1e-14)
+        assert names == ["counts", "dW"]
+
