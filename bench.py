@@ -548,7 +548,7 @@ def run_ours(args, w):
             "config": {"workload": workload_desc(w), "global_batch": ws * N, "seq_len": 4096 if N >= 4096 else N,
                        "parallelism": "dp%d" % ws if ws > 1 else "single",
                        "l2": "inputs larger than L2 (W %.0f MiB > 129 MB); no flush" % (W.numel() * 2 / 2**20),
-                       "chunk_budget_bytes": budget or (1 << 30),
+                       "chunk_budget_bytes": budget or (512 << 20),
                        "filter_threshold": args.filter_threshold, "sort_vocab": args.sort_vocab,
                        "compensated": args.compensated},
             # flops counted as the exact path's 8*N*Hd*V; a filtered run skips part of it

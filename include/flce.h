@@ -96,10 +96,12 @@ FLCE_API size_t flce_forward_workspace_size(int64_t N, int64_t Hd, int64_t V);
    holds a bf16 [Vc, Hd] copy of the chunk's weight rows in sorted order and the order
    itself (about 28 bytes per vocabulary row); with FLCE_BWD_COMPENSATED a second bf16
    [N, Vc] chunk (the rounding remainder of dZ).
-   chunk_budget_bytes bounds the dZ chunk(s) plus that weight copy (0 = default 1 GiB):
-   Vc = budget / (2 N, 4 N when compensated, + 2 Hd when sorting), rounded down to 256.
-   The same budget and options must be passed to flce_backward.  Unknown option bits:
-   returns 0. */
+   chunk_budget_bytes bounds the dZ chunk(s) plus that weight copy (0 = default 512 MiB):
+   at most budget / (2 N, 4 N when compensated, + 2 Hd when sorting) columns, rounded down
+   to 256; the vocabulary's 256-column tiles are dealt out over the fewest chunks that
+   bound allows, as evenly as whole tiles allow (widths differ by at most 256 columns), and
+   the widest chunk Vc sets the size.  The same budget and options must be passed to
+   flce_backward.  Unknown option bits: returns 0. */
 FLCE_API size_t flce_backward_workspace_size(int64_t N, int64_t Hd, int64_t V, size_t chunk_budget_bytes,
                                              unsigned options);
 

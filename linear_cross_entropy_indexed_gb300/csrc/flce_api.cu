@@ -41,7 +41,11 @@ constexpr int kPlanPairs = 76;   // SM pairs of a GB300 (152 SMs), for the plann
 // once per band, instead of H streaming past once per vocabulary tile when it does
 // not fit in L2 (N = 32768: 224 MiB).
 constexpr int kBandM = 16;
-constexpr size_t kDefaultChunkBudget = size_t(1) << 30;  // bf16 dZ chunk bytes
+// bf16 dZ chunk bytes.  Measured sustained on one GB300 (forward + backward per step,
+// 100-step runs at the power cap): 512 MiB runs the Llama-3-, Gemma-2- and packed-shaped
+// heads within 0.5% of 1 GiB for 44-47% less peak extra memory; 384 and 256 MiB cost
+// 0.6-1.7% and 1.1-2.7% (more launches, each with its own ramp and tail).
+constexpr size_t kDefaultChunkBudget = size_t(512) << 20;
 constexpr int kMaxDevices = 64;
 
 thread_local int t_last_cuda = 0;
@@ -255,8 +259,14 @@ bool plan_vocab(int64_t N, int64_t Hd, int64_t V, size_t* cur, VocabPlan* p) {
 }
 
 struct BwdPlan {
-  int64_t Vc = 0;
+  int64_t Vc = 0;              // widest chunk: the dZ buffer's row pitch in elements
   int n_chunks = 0;
+  int64_t v_tiles = 0;         // 256-column tiles of the vocabulary, split over the chunks
+  // Chunk c covers vocabulary columns [chunk_begin(c), chunk_begin(c + 1)): the tiles are
+  // dealt out as evenly as whole tiles allow, so widths differ by at most one tile.
+  int64_t chunk_begin(int c, int64_t V) const {
+    return c >= n_chunks ? V : (int64_t(c) * v_tiles / n_chunks) * kBN;
+  }
   int dh_split = 1;            // K parts per dH output tile (1: no split)
   int nz_rows = 0, nz_ld = 0;  // token blocks x vocabulary blocks of the dZ block flags
   int dh_mask_ld = 0, dw_mask_ld = 0, mask_tok_tiles = 0, mask_voc_tiles = 0;
@@ -290,8 +300,9 @@ int choose_dh_split(int64_t tiles, int pairs, int64_t k_blocks) {
 // The chunk budget covers the bf16 dZ chunk (two of them, value and rounding remainder, in
 // the compensated mode) and, with the sorted vocabulary, the bf16 copy of the chunk's
 // weight rows in sorted order: at most budget / (2N (x2) (+ 2Hd)) columns, a multiple of
-// 256.  The vocabulary is then cut into that many chunks of equal width (rounded up to
-// 256), so the last chunk is not a thin remainder with its own launch tails.
+// 256.  The vocabulary's 256-column tiles are then dealt out over the fewest chunks that
+// bound allows, as evenly as whole tiles allow, so the last chunk is not a thin remainder
+// with its own launch tails.
 flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, unsigned options, BwdPlan* p) {
   flce_status s = check_sizes(N, Hd, V);
   if (s != FLCE_OK) return s;
@@ -304,10 +315,10 @@ flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, unsig
   int64_t vc_max = N > 0 ? static_cast<int64_t>(std::min<size_t>(budget / per_col, size_t(v_round))) : v_round;
   vc_max = vc_max / kBN * kBN;
   if (vc_max < kBN) vc_max = kBN;
-  const int64_t want = cdiv(V, vc_max);                          // chunks the budget allows
-  const int64_t vc = int64_t(cdiv(cdiv(V, want), kBN)) * kBN;    // equal widths, <= vc_max
+  p->v_tiles = cdiv(V, kBN);
+  p->n_chunks = cdiv(V, vc_max);                                 // fewest chunks within the bound
+  const int64_t vc = int64_t(cdiv(p->v_tiles, p->n_chunks)) * kBN;  // widest chunk, <= vc_max
   p->Vc = vc;
-  p->n_chunks = cdiv(V, vc);
   // the compensated mode's two-part A operand is not split
   p->dh_split = p->split ? 1 : choose_dh_split(int64_t(cdiv(N, kPairM)) * cdiv(Hd, kBN), kPlanPairs, cdiv(vc, kBK));
   p->nz_rows = cdiv(N, 64);
@@ -561,8 +572,8 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
   const int m_tiles_tok = cdiv(N, kPairM);
   const int d_tiles = cdiv(Hd, kBN);
   for (int c = 0; c < pl.n_chunks; ++c) {
-    const int64_t v0 = int64_t(c) * pl.Vc;
-    const int64_t wc = std::min<int64_t>(pl.Vc, V - v0);
+    const int64_t v0 = pl.chunk_begin(c, V);
+    const int64_t wc = pl.chunk_begin(c + 1, V) - v0;
     CUtensorMap tmDz_k, tmDz_mn, tmLo_k, tmLo_mn;
     if (!tmap_2d(&tmDz_k, dz, wc, N, pl.Vc * 2, kBK, kBM) || !tmap_2d(&tmDz_mn, dz, wc, N, pl.Vc * 2, 64, kBK))
       return FLCE_ERR_CUDA;
