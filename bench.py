@@ -37,17 +37,21 @@ METRIC = "fused linear-CE fwd+bwd tokens/s at 1 GB300; % of bf16 tensor peak; pe
 L2_BYTES = 129 * 10**6
 
 # DRAM traffic per launch of the dominant kernel class from one ncu capture, keyed by
-# the hash of the kernel sources it was taken on (null once the sources change).
+# the kernel class, the workload, the backward chunk budget (a per-chunk launch's traffic
+# depends on its width) and the hash of the kernel sources it was taken on (null once the
+# sources change, or for a budget never captured).
 MEASURED_TRAFFIC = {
     # ncu capture of the four tensor-core kernels at the llama2 size (DRAM read + written
-    # per launch), scaled by tiles per launch to llama3: x 4.008 for the linear-LSE launch
-    # (501 / 125 vocabulary tiles), x 2.004 for the per-chunk dZ / dW / dH launches; both
-    # sizes have 32 token tiles, so the banded schedules stream W twice per launch in both
-    ("linear_lse", "llama3", "226080fb59c1dd05"): 3.31e9,   # 0.822 + 0.004 GB at llama2
-    ("dz", "llama3", "226080fb59c1dd05"): 2.38e9,           # 0.683 + 0.505 GB
-    ("dw", "llama3", "226080fb59c1dd05"): 5.12e9,           # 2.300 + 0.257 GB
-    ("dh", "llama3", "226080fb59c1dd05"): 5.03e9,           # 2.446 + 0.063 GB
+    # per launch), scaled by tiles per launch to llama3 with 1 GiB chunks: x 4.008 for the
+    # linear-LSE launch (501 / 125 vocabulary tiles), x 2.004 for the per-chunk dZ / dW / dH
+    # launches; both sizes have 32 token tiles, so the banded schedules stream W twice per
+    # launch in both
+    ("linear_lse", "llama3", 1 << 30, "226080fb59c1dd05"): 3.31e9,   # 0.822 + 0.004 GB at llama2
+    ("dz", "llama3", 1 << 30, "226080fb59c1dd05"): 2.38e9,           # 0.683 + 0.505 GB
+    ("dw", "llama3", 1 << 30, "226080fb59c1dd05"): 5.12e9,           # 2.300 + 0.257 GB
+    ("dh", "llama3", 1 << 30, "226080fb59c1dd05"): 5.03e9,           # 2.446 + 0.063 GB
 }
+DEFAULT_CHUNK_BUDGET = 512 << 20  # the library's default (flce_api.cu)
 
 
 # the sources that define the tensor-core kernels (engine, PTX wrappers, tile constants
@@ -421,7 +425,7 @@ def run_ours(args, w):
         per_launch_flops = flops_per_class[dom] * args.steps / launches_dom
         achieved = per_launch_flops / (per_launch_ms * 1e-3) / 1e12
         h = kernel_source_hash()
-        traffic = MEASURED_TRAFFIC.get((dom, w.name, h))
+        traffic = MEASURED_TRAFFIC.get((dom, w.name, budget or DEFAULT_CHUNK_BUDGET, h))
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_sus"], "traffic": traffic,
                 "peak_kind": "bf16_tflops_sustained (%s)" % peaks["source"],
@@ -548,7 +552,7 @@ def run_ours(args, w):
             "config": {"workload": workload_desc(w), "global_batch": ws * N, "seq_len": 4096 if N >= 4096 else N,
                        "parallelism": "dp%d" % ws if ws > 1 else "single",
                        "l2": "inputs larger than L2 (W %.0f MiB > 129 MB); no flush" % (W.numel() * 2 / 2**20),
-                       "chunk_budget_bytes": budget or (512 << 20),
+                       "chunk_budget_bytes": budget or DEFAULT_CHUNK_BUDGET,
                        "filter_threshold": args.filter_threshold, "sort_vocab": args.sort_vocab,
                        "compensated": args.compensated},
             # flops counted as the exact path's 8*N*Hd*V; a filtered run skips part of it

@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "flce.h"
+#include "host_internal.h"
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "small_kernels.cuh"

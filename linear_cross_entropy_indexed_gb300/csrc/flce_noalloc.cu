@@ -20,7 +20,7 @@
 #include <mutex>
 
 #include "flce.h"
-#include "internal.cuh"
+#include "host_internal.h"
 
 namespace {
 

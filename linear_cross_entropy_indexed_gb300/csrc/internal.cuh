@@ -127,11 +127,4 @@ cudaError_t launch_dh(const CUtensorMap& tmDz, const CUtensorMap& tmDz2, const C
 cudaError_t set_gemm_smem_attributes_fwd();
 cudaError_t set_gemm_smem_attributes_bwd();
 
-// Host helpers shared by the entry-point translation units (defined in flce_api.cu).
-// check_device: the current device is one the library runs on (sm_103), with the same
-// status every entry point returns.  record_cuda_error: remembers e for
-// flce_last_cuda_error() and returns FLCE_ERR_CUDA.
-int check_device();
-int record_cuda_error(cudaError_t e);
-
 }  // namespace flce

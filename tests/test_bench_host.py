@@ -50,5 +50,6 @@ def test_unparsable_lines_are_skipped():
 def test_kernel_source_hash_is_stable_and_short():
     h = bench.kernel_source_hash()
     assert h == bench.kernel_source_hash() and len(h) == 16
-    # the traffic table is keyed by that hash: a stale entry reads as unmeasured (null)
-    assert all(len(k[2]) == 16 for k in bench.MEASURED_TRAFFIC)
+    # the traffic table is keyed by kernel class, workload, chunk budget and that hash: a
+    # stale entry, or a budget never captured, reads as unmeasured (null)
+    assert all(len(k) == 4 and isinstance(k[2], int) and len(k[3]) == 16 for k in bench.MEASURED_TRAFFIC)
