@@ -50,6 +50,12 @@ MEASURED_TRAFFIC = {
     ("dz", "llama3", 1 << 30, "226080fb59c1dd05"): 2.38e9,           # 0.683 + 0.505 GB
     ("dw", "llama3", 1 << 30, "226080fb59c1dd05"): 5.12e9,           # 2.300 + 0.257 GB
     ("dh", "llama3", 1 << 30, "226080fb59c1dd05"): 5.03e9,           # 2.446 + 0.063 GB
+    # direct ncu capture at llama3 with the 512 MiB default (4 chunks of 126 / 125
+    # vocabulary tiles), mean of two launches per kernel, DRAM read + written
+    ("linear_lse", "llama3", 512 << 20, "226080fb59c1dd05"): 4.43e9,  # 4.421 + 0.010 GB
+    ("dz", "llama3", 512 << 20, "226080fb59c1dd05"): 1.19e9,          # 0.685 + 0.506 GB
+    ("dw", "llama3", 512 << 20, "226080fb59c1dd05"): 2.60e9,          # 2.342 + 0.256 GB
+    ("dh", "llama3", 512 << 20, "226080fb59c1dd05"): 2.68e9,          # 2.586 + 0.091 GB
 }
 DEFAULT_CHUNK_BUDGET = 512 << 20  # the library's default (flce_api.cu)
 
