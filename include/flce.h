@@ -85,7 +85,11 @@ typedef enum flce_reduction {
    Returns 0 and sets no error for invalid sizes; flce_forward reports those. */
 FLCE_API size_t flce_forward_workspace_size(int64_t N, int64_t Hd, int64_t V);
 
-/* Bytes of scratch that flce_backward needs.  The backward walks the vocabulary in
+/* Bytes of scratch that flce_backward needs.  The backward runs on the rows that carry
+   a gradient only (a valid label and a non-zero upstream gradient; every other row's
+   gradient is exactly zero): it gathers them, in order, into a compact bf16 copy of H
+   (N rounded up to 256 rows) with their per-row data and a row map, and their count stays
+   on the device.  It walks the vocabulary in
    chunks of Vc columns and keeps one bf16 [N, Vc] dZ chunk plus an fp32 [N, Hd] dH
    accumulator (the latter only when there is more than one chunk, or when dH is split),
    plus one byte per 64 x 64 block of the chunk for the filtered mode.  When the dH
@@ -298,6 +302,8 @@ FLCE_API int flce_last_cuda_error(void);
 #define FLCE_KERNEL_VOCAB_SORT 13  /* run sort + merge passes -> perm / inv               */
 #define FLCE_KERNEL_GATHER 14      /* sorted chunk's weight rows -> contiguous copy       */
 #define FLCE_KERNEL_DH_COMBINE 15  /* dH split: fp32 part sums added in part order        */
+#define FLCE_KERNEL_COMPACT 16     /* backward: rows with a gradient gathered to the front  */
+#define FLCE_KERNEL_DH_ZERO 17     /* backward: zero dH rows that carry no gradient         */
 FLCE_API uint64_t flce_launch_count(void);
 FLCE_API int flce_set_event_sink(void* const* start_events, void* const* end_events, int* kernel_ids,
                         int capacity);

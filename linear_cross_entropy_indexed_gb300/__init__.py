@@ -36,7 +36,8 @@ __all__ = [
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 KERNEL_NAMES = {0: "label_dot", 1: "linear_lse", 2: "lse_merge", 3: "reduce", 4: "bwd_prep",
                 5: "dz", 6: "dw", 7: "dh", 8: "zero", 9: "block_mask", 10: "selftest", 11: "shard_merge",
-                12: "vocab_keys", 13: "vocab_sort", 14: "gather", 15: "dh_combine"}
+                12: "vocab_keys", 13: "vocab_sort", 14: "gather", 15: "dh_combine", 16: "compact",
+                17: "dh_zero"}
 BWD_SORT_VOCAB = 1
 BWD_COMPENSATED = 2
 

@@ -275,6 +275,11 @@ struct BwdPlan {
   VocabPlan vocab;
   size_t off_rows = 0, off_dz = 0, off_dz_lo = 0, off_dh = 0, off_dh_parts = 0, off_nz = 0, off_dh_mask = 0,
          off_dw_mask = 0, off_wperm = 0, total = 0;
+  // row compaction: compact RowInfo [n_cap], row map [N], compact H [n_cap][Hd] bf16,
+  // per-block counts and the compact row count
+  int64_t n_cap = 0;
+  int compact_blocks = 0;
+  size_t off_rows_c = 0, off_map = 0, off_hc = 0, off_blk = 0, off_nrows = 0;
 };
 
 // K parts per dH output tile: the count (1 .. kMaxDhSplit, at most the chunk's K blocks)
@@ -333,6 +338,14 @@ flce_status plan_backward(int64_t N, int64_t Hd, int64_t V, size_t budget, unsig
   if ((p->n_chunks > 1 || p->dh_split > 1) && (!mul_ok(size_t(N), size_t(Hd), &dh) || !mul_ok(dh, 4, &dh)))
     return FLCE_ERR_OVERFLOW;
   if (p->dh_split > 1 && !mul_ok(dh, size_t(p->dh_split - 1), &parts)) return FLCE_ERR_OVERFLOW;
+  p->n_cap = int64_t(cdiv(N, kPairM)) * kPairM;
+  p->compact_blocks = std::max(cdiv(N, kCompactRows), 1);
+  size_t hc;
+  if (!mul_ok(size_t(p->n_cap), size_t(Hd), &hc) || !mul_ok(hc, 2, &hc)) return FLCE_ERR_OVERFLOW;
+  if (!reserve(&cur, size_t(p->n_cap) * sizeof(RowInfo), &p->off_rows_c) ||
+      !reserve(&cur, size_t(N) * 4, &p->off_map) || !reserve(&cur, hc, &p->off_hc) ||
+      !reserve(&cur, size_t(p->compact_blocks) * 4, &p->off_blk) || !reserve(&cur, 4, &p->off_nrows))
+    return FLCE_ERR_OVERFLOW;
   if (!reserve(&cur, size_t(N) * sizeof(RowInfo), &p->off_rows) || !reserve(&cur, dz, &p->off_dz) ||
       !reserve(&cur, p->split ? dz : 0, &p->off_dz_lo) || !reserve(&cur, dh, &p->off_dh) ||
       !reserve(&cur, parts, &p->off_dh_parts) || !reserve(&cur, size_t(p->nz_rows) * size_t(p->nz_ld), &p->off_nz) ||
@@ -565,8 +578,49 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
   });
   if (e != cudaSuccess) return cuda_fail(e);
 
+  // Row compaction: the rows that carry a gradient (scale != 0) are gathered to the front of
+  // a compact copy of H, in their original order, with their RowInfo; their count stays on
+  // the device, where the tensor-core kernels read it.  Every other row contributes exact
+  // zeros (its dZ row is zero), so the products run on the compact rows only and dH is
+  // scattered back through the row map; the other rows of dH are written as zeros here.
+  RowInfo* rows_c = reinterpret_cast<RowInfo*>(ws + pl.off_rows_c);
+  int32_t* rmap = reinterpret_cast<int32_t*>(ws + pl.off_map);
+  __nv_bfloat16* Hc = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_hc);
+  int* blk = reinterpret_cast<int*>(ws + pl.off_blk);
+  int* n_rows = reinterpret_cast<int*>(ws + pl.off_nrows);
+  const auto* Hb = static_cast<const __nv_bfloat16*>(H);
+  e = launch(FLCE_KERNEL_COMPACT, st, [&] {
+    k_compact_count<<<pl.compact_blocks, kCompactRows, 0, st>>>(rows, N, blk);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch(FLCE_KERNEL_COMPACT, st, [&] {
+    k_compact_scan<<<1, kCompactRows, 0, st>>>(blk, pl.compact_blocks, n_rows);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch(FLCE_KERNEL_COMPACT, st, [&] {
+    k_compact_place<<<pl.compact_blocks, kCompactRows, 0, st>>>(rows, N, blk, rmap, rows_c);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch(FLCE_KERNEL_COMPACT, st, [&] {
+    k_compact_gather<<<static_cast<int>(std::min<int64_t>(cdiv(pl.n_cap, 8), 8 * int64_t(sms))), 256, 0, st>>>(
+        Hb, N, Hd, rmap, n_rows, pl.n_cap, Hc, rows_c);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (want_dh) {
+    e = launch(FLCE_KERNEL_DH_ZERO, st, [&] {
+      k_zero_dead_rows<<<static_cast<int>(std::min<int64_t>(cdiv(N, 8), 8 * int64_t(sms))), 256, 0, st>>>(
+          rows, N, Hd, static_cast<__nv_bfloat16*>(dH), dh_partial);
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+
   CUtensorMap tmH_k, tmW_k, tmH_mn, tmW_mn;
-  if (!tmap_2d(&tmH_k, H, Hd, N, Hd * 2, kBK, kBM) || !tmap_2d(&tmH_mn, H, Hd, N, Hd * 2, 64, kBK) ||
+  if (!tmap_2d(&tmH_k, Hc, Hd, pl.n_cap, Hd * 2, kBK, kBM) || !tmap_2d(&tmH_mn, Hc, Hd, pl.n_cap, Hd * 2, 64, kBK) ||
       (!pl.sort && (!tmap_2d(&tmW_k, W, Hd, V, Hd * 2, kBK, kBN / 2) || !tmap_2d(&tmW_mn, W, Hd, V, Hd * 2, 64, kBK))))
     return FLCE_ERR_CUDA;
 
@@ -609,9 +663,11 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
     s4.order = 0;
     s4.band = kBandM;
     s4.b_n_off = static_cast<int>(w_off);
+    s4.n_dev = n_rows;  // M walks the compact rows
+    s4.n_role = 1;
     if (filter && (e = cudaMemsetAsync(nz, 0, size_t(pl.nz_rows) * size_t(pl.nz_ld), st)) != cudaSuccess)
       return cuda_fail(e);
-    EpiDzParams p4{N, V, v0, wc, pl.Vc, softcap, rows, dz, dz_lo, filter_threshold, nz, pl.nz_ld};
+    EpiDzParams p4{N, V, v0, wc, pl.Vc, softcap, rows_c, dz, dz_lo, filter_threshold, nz, pl.nz_ld};
     e = launch(FLCE_KERNEL_DZ, st,
                [&] { return launch_dz(tmH_k, tmW_k, s4, p4, err, pair_grid(s4.units, sms), st); });
     if (e != cudaSuccess) return cuda_fail(e);
@@ -637,6 +693,8 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
     s5.n_groups = d_tiles;
     s5.units = s5.m_tiles * s5.n_groups;
     s5.order = 1;
+    s5.n_dev = n_rows;  // K walks the compact rows
+    s5.n_role = 2;
     if (skip) {
       s5.kmask = dw_mask;
       s5.kmask_ld = pl.dw_mask_ld;
@@ -662,6 +720,8 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
     s6.units = s6.m_tiles * s6.n_groups;
     s6.order = 1;
     s6.b_k_off = static_cast<int>(w_off);
+    s6.n_dev = n_rows;  // M walks the compact rows
+    s6.n_role = 1;
     if (skip) {
       s6.kmask = dh_mask;
       s6.kmask_ld = pl.dh_mask_ld;
@@ -670,15 +730,17 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
       s6.k_half = s6.k_blocks;
       s6.k_blocks *= 2;
     }
-    // K split of the exact product (the filtered mode keeps whole tiles for its K-step masks)
-    const int ksplit = filter ? 1 : std::min(pl.dh_split, s6.k_blocks);
+    // K split of the exact product (the filtered mode keeps whole tiles for its K-step masks;
+    // a shard's fp32 partial is accumulated in dH's own rows, without part sums)
+    const int ksplit = (filter || dh_partial != nullptr) ? 1 : std::min(pl.dh_split, s6.k_blocks);
     s6.k_split = ksplit;
     s6.units *= ksplit;
     float* dh_acc = dh_partial != nullptr ? dh_partial : dh32;
     const bool last = c == pl.n_chunks - 1;
     EpiDhParams p6 = dh_partial != nullptr
-                         ? EpiDhParams{N, Hd, dh_partial, nullptr, c == 0, 0, dh_parts}
-                         : EpiDhParams{N, Hd, dh32, static_cast<__nv_bfloat16*>(dH), c == 0, last && ksplit == 1, dh_parts};
+                         ? EpiDhParams{N, Hd, dh_partial, nullptr, c == 0, 0, dh_parts, rmap, n_rows, 1}
+                         : EpiDhParams{N, Hd, dh32, static_cast<__nv_bfloat16*>(dH), c == 0, last && ksplit == 1,
+                                       dh_parts, rmap, n_rows, 0};
     if (want_dh) {
       e = launch(FLCE_KERNEL_DH, st,
                  [&] { return launch_dh(tmDz_k, tmLo_k, tmW_mn, s6, p6, err, pair_grid(s6.units, sms), st); });
@@ -688,7 +750,7 @@ flce_status backward_impl(const void* H, const void* W, const int64_t* labels, c
         const int64_t count = N * Hd;
         e = launch(FLCE_KERNEL_DH_COMBINE, st, [&] {
           k_dh_combine<<<static_cast<int>(std::min<int64_t>(std::max<int64_t>(count / 4 / 256, 1), 8 * sms)), 256, 0,
-                         st>>>(dh_acc, dh_parts, ksplit - 1, count, out);
+                         st>>>(dh_acc, dh_parts, ksplit - 1, count, Hd, out, rmap, n_rows);
           return cudaGetLastError();
         });
         if (e != cudaSuccess) return cuda_fail(e);

@@ -65,6 +65,13 @@ struct Sched {
   // steps [k_half, 2 k_half) the same coordinates through the second; B is read at the
   // step index modulo k_half, so the accumulator sums A1 B + A2 B.
   int k_half;
+  // Token extent read on the device at launch (null: the fields above stand).  The
+  // backward runs on the rows that carry a gradient, compacted to the front; their count
+  // is known only on the device.  n_role 1: M walks those rows, m_tiles = max(1,
+  // ceil(n / 256)) and units = k_split * m_tiles * n_groups; n_role 2: K walks them,
+  // k_blocks = max(1, ceil(n / 64)) (doubled with a two-part A operand).
+  const int* n_dev;
+  int n_role;
 };
 
 // Per-row data the dZ epilogue needs, packed in one 16-byte load.
@@ -107,10 +114,16 @@ struct EpiDwParams {
 
 struct EpiDhParams {
   int64_t N, Hd;
-  float* acc32;         // [N, Hd] fp32 running sum across vocabulary chunks
-  __nv_bfloat16* out;   // dH
+  float* acc32;         // [N, Hd] fp32 running sum across vocabulary chunks (compact rows)
+  __nv_bfloat16* out;   // dH (rows of the original order)
   int first, last;
   float* parts;         // K split: fp32 sums of K parts 1 .. k_split - 1, [k_split - 1][N][Hd]
+  // Compact rows: row r < *n_rows of the product is row row_map[r] of dH; rows from
+  // *n_rows on are not written to dH.  Null: rows are dH's own.  acc_mapped: the running
+  // sum acc32 is in dH's rows too (the fp32 partial of a vocabulary shard), else compact.
+  const int32_t* row_map;
+  const int* n_rows;
+  int acc_mapped;
 };
 
 // Launchers (defined in the kernel translation units).  Each returns the launch error.

@@ -137,14 +137,25 @@ __global__ void __launch_bounds__(kMergeRows * kMergeSlices)
 }
 
 // dH split: acc += parts[0] + parts[1] + ... in part order, 4 elements per thread per
-// step (16-byte loads; count = N Hd is a multiple of 8).  At the last vocabulary chunk
-// (out != null) the sum goes to the bf16 dH instead of back into the running sum.
+// step (16-byte loads; count = N Hd, Hd a multiple of 8).  At the last vocabulary chunk
+// (out != null) the sum goes to the bf16 dH instead of back into the running sum: the
+// rows are compact, row r < *n_rows going to dH row row_map[r] (rows past *n_rows hold
+// no gradient and are not written).
 __global__ void __launch_bounds__(256)
-    k_dh_combine(float* __restrict__ acc, const float* __restrict__ parts, int n_parts, int64_t count,
-                 __nv_bfloat16* __restrict__ out) {
+    k_dh_combine(float* __restrict__ acc, const float* __restrict__ parts, int n_parts, int64_t count, int64_t Hd,
+                 __nv_bfloat16* __restrict__ out, const int32_t* __restrict__ row_map, const int* __restrict__ n_rows) {
   const int64_t n4 = count / 4;
+  const int64_t nr = (out != nullptr && row_map != nullptr) ? static_cast<int64_t>(*n_rows) : 0;
   for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < n4;
        q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    int64_t oq = q;  // destination float4 index (in dH's rows)
+    if (out != nullptr && row_map != nullptr) {
+      const int64_t r = (4 * q) / Hd;
+      if (r >= nr) continue;
+      const int64_t o = row_map[r];
+      if (o < 0 || o >= count / Hd) continue;
+      oq = (o * Hd + (4 * q - r * Hd)) / 4;
+    }
     float4 v = reinterpret_cast<const float4*>(acc)[q];
     for (int j = 0; j < n_parts; ++j) {
       const float4 w = reinterpret_cast<const float4*>(parts + static_cast<int64_t>(j) * count)[q];
@@ -159,9 +170,127 @@ __global__ void __launch_bounds__(256)
       uint2 packed;
       packed.x = *reinterpret_cast<const uint32_t*>(&lo);
       packed.y = *reinterpret_cast<const uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(out)[q] = packed;
+      reinterpret_cast<uint2*>(out)[oq] = packed;
     } else {
       reinterpret_cast<float4*>(acc)[q] = v;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ row compaction
+// The backward runs only on the rows that carry a gradient (scale != 0: a valid label and
+// a non-zero upstream gradient); every other row's dZ row, dH row and share of dW are
+// exactly zero.  The rows that do are gathered to the front in their original order: a
+// count per block of kCompactRows rows, an exclusive scan of the counts (one block), then
+// each row's place.  The count of such rows stays on the device.
+constexpr int kCompactRows = 1024;
+
+__global__ void __launch_bounds__(kCompactRows)
+    k_compact_count(const RowInfo* __restrict__ rows, int64_t N, int* __restrict__ blk_cnt) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kCompactRows + threadIdx.x;
+  const int live = (i < N && rows[i].scale != 0.0f) ? 1 : 0;
+  const int c = __syncthreads_count(live);
+  if (threadIdx.x == 0) blk_cnt[blockIdx.x] = c;
+}
+
+// Exclusive scan of nblk block counts in place (blocks of kCompactRows values, each
+// scanned in shared memory, carried in order); the total goes to *n_rows.
+__global__ void __launch_bounds__(kCompactRows) k_compact_scan(int* __restrict__ blk, int nblk, int* __restrict__ n_rows) {
+  __shared__ int sh[kCompactRows];
+  __shared__ int carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < nblk; base += kCompactRows) {
+    const int k = base + static_cast<int>(threadIdx.x);
+    const int v = k < nblk ? blk[k] : 0;
+    sh[threadIdx.x] = v;
+    __syncthreads();
+    for (int off = 1; off < kCompactRows; off <<= 1) {  // inclusive Hillis-Steele scan
+      const int t = threadIdx.x >= static_cast<unsigned>(off) ? sh[threadIdx.x - off] : 0;
+      __syncthreads();
+      sh[threadIdx.x] += t;
+      __syncthreads();
+    }
+    if (k < nblk) blk[k] = carry + sh[threadIdx.x] - v;
+    __syncthreads();
+    if (threadIdx.x == kCompactRows - 1) carry += sh[threadIdx.x];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *n_rows = carry;
+}
+
+// Row i that carries a gradient goes to position blk_off[block] + its rank in the block:
+// map[pos] = i, rows_c[pos] = rows[i].
+__global__ void __launch_bounds__(kCompactRows)
+    k_compact_place(const RowInfo* __restrict__ rows, int64_t N, const int* __restrict__ blk_off,
+                    int32_t* __restrict__ map, RowInfo* __restrict__ rows_c) {
+  __shared__ int warp_sum[kCompactRows / 32];
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kCompactRows + threadIdx.x;
+  const bool live = i < N && rows[i].scale != 0.0f;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const unsigned ball = __ballot_sync(0xffffffffu, live);
+  if (lane == 0) warp_sum[w] = __popc(ball);
+  __syncthreads();
+  if (w == 0) {  // exclusive scan of the 32 warp sums
+    const int v = warp_sum[lane];
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    warp_sum[lane] = incl - v;
+  }
+  __syncthreads();
+  if (live) {
+    const int pos = blk_off[blockIdx.x] + warp_sum[w] + __popc(ball & ((1u << lane) - 1u));
+    map[pos] = static_cast<int32_t>(i);
+    rows_c[pos] = rows[i];
+  }
+}
+
+// One warp per compact row p < ceil256(max(n, 1)) (n = *n_rows), bounded by n_cap: rows
+// p < n copy H row map[p] into Hc row p; the rest of the last 256-row tile is zeroed
+// (Hc and rows_c: no gradient, finite logits), so that the tile computes exact zeros.
+__global__ void __launch_bounds__(256)
+    k_compact_gather(const __nv_bfloat16* __restrict__ H, int64_t N, int64_t Hd, const int32_t* __restrict__ map,
+                     const int* __restrict__ n_rows, int64_t n_cap, __nv_bfloat16* __restrict__ Hc,
+                     RowInfo* __restrict__ rows_c) {
+  const int64_t n = *n_rows;
+  const int64_t end = min(n_cap, ((max(n, int64_t(1)) + 255) / 256) * 256);
+  const int lane = threadIdx.x & 31;
+  const int64_t vec = Hd / 8;
+  for (int64_t p = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; p < end;
+       p += static_cast<int64_t>(gridDim.x) * blockDim.x / 32) {
+    uint4* dst = reinterpret_cast<uint4*>(Hc + p * Hd);
+    if (p < n) {
+      const int64_t src_row = map[p];
+      if (src_row < 0 || src_row >= N) continue;  // (never: map holds rows of H)
+      const uint4* src = reinterpret_cast<const uint4*>(H + src_row * Hd);
+      for (int64_t k = lane; k < vec; k += 32) dst[k] = __ldg(src + k);
+    } else {
+      for (int64_t k = lane; k < vec; k += 32) dst[k] = make_uint4(0u, 0u, 0u, 0u);
+      if (lane == 0) rows_c[p] = RowInfo{0.0f, 0.0f, -1, 0};
+    }
+  }
+}
+
+// Rows that carry no gradient get an exactly zero output row: one warp per row, bf16 dH
+// or fp32 dH partial (whichever is given).
+__global__ void __launch_bounds__(256)
+    k_zero_dead_rows(const RowInfo* __restrict__ rows, int64_t N, int64_t Hd, __nv_bfloat16* __restrict__ dh_bf16,
+                     float* __restrict__ dh_f32) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; i < N;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x / 32) {
+    if (rows[i].scale != 0.0f) continue;
+    if (dh_bf16 != nullptr) {
+      uint4* d = reinterpret_cast<uint4*>(dh_bf16 + i * Hd);
+      for (int64_t k = lane; k < Hd / 8; k += 32) d[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (dh_f32 != nullptr) {
+      float4* d = reinterpret_cast<float4*>(dh_f32 + i * Hd);
+      for (int64_t k = lane; k < Hd / 4; k += 32) d[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }

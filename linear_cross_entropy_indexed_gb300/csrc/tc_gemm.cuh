@@ -323,13 +323,26 @@ struct EpiDh {
       p.acc32 = pp.parts + static_cast<int64_t>(ks - 1) * pp.N * pp.Hd;
       p.first = 1;
       p.last = 0;
+      p.acc_mapped = 0;
     }
     const int lane = threadIdx.x & 31;
     const int64_t mine = row < p.N ? row : -1;
+    // the row of dH this product row lands in (compact rows: through the row map; rows
+    // past the compact count hold no gradient and land nowhere)
+    int64_t out_mine = mine, acc_mine = mine;
+    if (p.row_map != nullptr && (p.last || p.acc_mapped)) {
+      const int64_t nr = *p.n_rows;
+      const int64_t o = (mine >= 0 && row < nr) ? static_cast<int64_t>(p.row_map[row]) : -1;
+      out_mine = (o >= 0 && o < p.N) ? o : -1;
+      if (p.acc_mapped) acc_mine = out_mine;
+    }
     // step i moves rows 4i .. 4i+3 of the warp: lane -> row 4i + lane/8, 4-column chunk lane%8
-    int64_t dst[8];
+    int64_t dst[8], odst[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) dst[i] = __shfl_sync(0xffffffffu, mine, 4 * i + (lane >> 3));
+    for (int i = 0; i < 8; ++i) {
+      dst[i] = __shfl_sync(0xffffffffu, acc_mine, 4 * i + (lane >> 3));
+      odst[i] = __shfl_sync(0xffffffffu, out_mine, 4 * i + (lane >> 3));
+    }
     const int ch = lane & 7;
     const int64_t col_tile = static_cast<int64_t>(nt) * kBN;
     const int c_end = (h + 1) * kSlicesPerWarp;
@@ -369,7 +382,9 @@ struct EpiDh {
           v.w += cur[i].w;
         }
         if (p.last) {
-          *reinterpret_cast<uint2*>(p.out + dst[i] * p.Hd + cc) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+          if (odst[i] >= 0)
+            *reinterpret_cast<uint2*>(p.out + odst[i] * p.Hd + cc) =
+                make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
         } else {
           *reinterpret_cast<float4*>(p.acc32 + dst[i] * p.Hd + cc) = v;
         }
@@ -434,8 +449,25 @@ template <class Epi, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB,
-                        const Sched sched, const typename Epi::Params ep, unsigned long long* err) {
+                        const Sched sched_in, const typename Epi::Params ep, unsigned long long* err) {
   extern __shared__ uint8_t smem_raw[];
+  // the token extent of a compacted backward is read here, before any role uses the schedule
+  Sched sched = sched_in;
+  if (sched.n_dev != nullptr) {
+    const int n = max(0, *sched.n_dev);
+    if (sched.n_role == 1) {
+      sched.m_tiles = max(1, (n + kPairM - 1) / kPairM);
+      sched.units = (sched.k_split > 1 ? sched.k_split : 1) * sched.m_tiles * sched.n_groups;
+    } else if (sched.n_role == 2) {
+      const int kb = max(1, (n + kBK - 1) / kBK);
+      if (sched.k_half > 0) {
+        sched.k_half = kb;
+        sched.k_blocks = 2 * kb;
+      } else {
+        sched.k_blocks = kb;
+      }
+    }
+  }
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStageBytes);

@@ -60,49 +60,54 @@ def test_workspace_sizes(lib):
     tiles = -(-v // 256)
     assert f(n, hd, v) >= 2 * (-(-tiles // 8)) * n * 4
     assert f(n, hd, v) < 2 * (-(-tiles // 4)) * n * 4 + (1 << 20)
-    # backward: one bf16 [N, Vc] chunk plus an fp32 [N, Hd] accumulator when chunked, and
-    # one byte per 64 x 64 block of the chunk for the filtered mode
+    # backward: one bf16 [N, Vc] chunk plus an fp32 [N, Hd] accumulator when chunked, one
+    # byte per 64 x 64 block of the chunk for the filtered mode, and the row compaction
+    # (the rows that carry a gradient gathered to the front): a bf16 copy of H and RowInfo
+    # for N rounded up to a 256-row tile, a row map, per-1024-row counts and the count
+    def compact(n_, hd_):
+        cap = -(-n_ // 256) * 256
+        return cap * hd_ * 2 + cap * 16 + n_ * 4 + max(-(-n_ // 1024), 1) * 4 + 4
     budget = 64 << 20
     vc = (budget // (2 * n)) // 256 * 256
     size = b(n, hd, v, budget, 0)
     flags = (n // 64) * (vc // 64)
-    assert size >= n * vc * 2 + n * hd * 4 + n * 16 + flags
-    assert size < n * vc * 2 + n * hd * 4 + n * 16 + flags + (1 << 12)
+    assert size >= n * vc * 2 + n * hd * 4 + n * 16 + flags + compact(n, hd)
+    assert size < n * vc * 2 + n * hd * 4 + n * 16 + flags + compact(n, hd) + (1 << 12)
     # chunks of equal width: a 1 GiB budget allows 65536 columns, so V = 128256 takes two
     # chunks, each ceil(128256 / 2) = 64128 columns rounded up to 256 = 64256
     size_1g = b(n, hd, v, 1 << 30, 0)
-    base_1g = n * 64256 * 2 + n * hd * 4 + n * 16 + (n // 64) * (64256 // 64)
+    base_1g = n * 64256 * 2 + n * hd * 4 + n * 16 + (n // 64) * (64256 // 64) + compact(n, hd)
     assert base_1g <= size_1g < base_1g + (1 << 14)  # + the K-step masks of the filtered mode
     # a single chunk needs no fp32 accumulator when dH is not split: 8192 x 4096 has 512 dH
     # tiles of 256 x 256, which fill 76 SM pairs to within 4%, so it is not split
     one = b(n, hd, 2000, 0, 0)
-    flags1 = (n // 64) * (2048 // 64)
+    flags1 = (n // 64) * (2048 // 64) + compact(n, hd)
     assert n * 2048 * 2 + n * 16 + flags1 <= one < n * 2048 * 2 + n * 16 + flags1 + (1 << 12)
     # few dH tiles: each tile's vocabulary range is split (256 x 64 is one tile: 4 parts),
     # which needs the fp32 accumulator and three fp32 [N, Hd] part sums even for one chunk
     small = b(256, 64, 2000, 0, 0)
-    base_s = 256 * 2048 * 2 + 256 * 16 + 4 * 256 * 64 * 4
+    base_s = 256 * 2048 * 2 + 256 * 16 + 4 * 256 * 64 * 4 + compact(256, 64)
     assert base_s <= small < base_s + (256 // 64) * (2048 // 64) + (1 << 12)
     # 4096 x 4096: 256 tiles, split in 2 (4 waves of 76 pairs -> 3.5): one part buffer
     v2 = (budget // (2 * 4096)) // 256 * 256
     two = b(4096, 4096, v, budget, 0)
-    base_2 = 4096 * v2 * 2 + 4096 * 16 + 2 * 4096 * 4096 * 4 + (4096 // 64) * (v2 // 64)
+    base_2 = 4096 * v2 * 2 + 4096 * 16 + 2 * 4096 * 4096 * 4 + (4096 // 64) * (v2 // 64) + compact(4096, 4096)
     assert base_2 <= two < base_2 + (1 << 13)
     # the compensated mode is never split
-    assert b(256, 64, 2000, 0, 2) < 2 * 256 * 2048 * 2 + 256 * 16 + (1 << 13)
+    assert b(256, 64, 2000, 0, 2) < 2 * 256 * 2048 * 2 + 256 * 16 + compact(256, 64) + (1 << 13)
     # the sorted vocabulary: the budget also covers the sorted bf16 weight rows of the
     # chunk, Vc = budget / (2N + 2Hd), plus the order (key, two sort words, perm, inv:
     # 28 bytes per vocabulary row) and the column sums of H
     vs = (budget // (2 * n + 2 * hd)) // 256 * 256
     flags_s = (n // 64) * (vs // 64)
     size_s = b(n, hd, v, budget, 1)
-    base = n * vs * 2 + vs * hd * 2 + n * hd * 4 + n * 16 + flags_s + 28 * v + 128 * hd * 4 + hd * 4
+    base = n * vs * 2 + vs * hd * 2 + n * hd * 4 + n * 16 + flags_s + 28 * v + 128 * hd * 4 + hd * 4 + compact(n, hd)
     assert base <= size_s < base + (1 << 13)
     assert b(n, hd, v, budget, 4) == 0 and b(n, hd, v, budget, 0x80000000) == 0
     # compensated: two bf16 dZ chunks, Vc = budget / 4N
     vcc = (budget // (4 * n)) // 256 * 256
     size_c = b(n, hd, v, budget, 2)
-    base_c = 2 * n * vcc * 2 + n * hd * 4 + n * 16 + (n // 64) * (vcc // 64)
+    base_c = 2 * n * vcc * 2 + n * hd * 4 + n * 16 + (n // 64) * (vcc // 64) + compact(n, hd)
     assert base_c <= size_c < base_c + (1 << 13)
     o = lib.flce_vocab_order_workspace_size
     assert 28 * v + 128 * hd * 4 + hd * 4 <= o(n, hd, v) < 28 * v + 128 * hd * 4 + hd * 4 + (1 << 12)

@@ -96,8 +96,9 @@ def test_step_captured_in_a_cuda_graph(mode):
 def test_skipping_a_gradient():
     """dW or dH can be skipped (NULL at the ABI): the other one is bit-identical to a full
     backward and the skipped gradient's kernels are not launched (per vocabulary chunk the
-    dW product, or the dH product and, when dH is split, its combining pass); autograd asks
-    for dH only when the weight is frozen."""
+    dW product, or the dH product and, when dH is split, its combining pass, and the zeroing
+    of the dH rows that carry no gradient); autograd asks for dH only when the weight is
+    frozen."""
     import linear_cross_entropy_indexed_gb300 as F
     w = S.scaled("llama3", N=300, Hd=128, V=3000, seed=61, w_std=0.05)
     Hb, Wb, y = P.make_case(w)
@@ -121,7 +122,7 @@ def test_skipping_a_gradient():
     assert torch.equal(dH_only, dH) and torch.equal(dW_only, dW)
     assert full.count("dw") == 3 and full.count("dh") == 3
     assert h_only == [k for k in full if k != "dw"]
-    assert w_only == [k for k in full if k not in ("dh", "dh_combine")]
+    assert w_only == [k for k in full if k not in ("dh", "dh_combine", "dh_zero")]
     with pytest.raises(F.FlceError, match="nothing to compute"):
         F.flce_backward(H, W, lab, lse, counts, g, compute_dH=False, compute_dW=False)
     # autograd with a frozen weight: H.grad matches, no dW launched
