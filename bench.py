@@ -56,6 +56,12 @@ MEASURED_TRAFFIC = {
     ("dz", "llama3", 512 << 20, "226080fb59c1dd05"): 1.19e9,          # 0.685 + 0.506 GB
     ("dw", "llama3", 512 << 20, "226080fb59c1dd05"): 2.60e9,          # 2.342 + 0.256 GB
     ("dh", "llama3", 512 << 20, "226080fb59c1dd05"): 2.68e9,          # 2.586 + 0.091 GB
+    # the same capture after the backward's row compaction (dZ and dH walk 31 of 32 token
+    # tiles and dW 122 of 128 K steps at the llama3 workload's 7756 rows with a gradient)
+    ("linear_lse", "llama3", 512 << 20, "be3b667aaba63e36"): 6.46e9,  # 6.454 + 0.010 GB
+    ("dz", "llama3", 512 << 20, "be3b667aaba63e36"): 1.20e9,          # 0.716 + 0.488 GB
+    ("dw", "llama3", 512 << 20, "be3b667aaba63e36"): 2.26e9,          # 2.010 + 0.255 GB
+    ("dh", "llama3", 512 << 20, "be3b667aaba63e36"): 2.66e9,          # 2.570 + 0.092 GB
 }
 DEFAULT_CHUNK_BUDGET = 512 << 20  # the library's default (flce_api.cu)
 
