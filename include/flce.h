@@ -264,6 +264,25 @@ FLCE_API flce_status flce_backward_shard(const void* H, const void* W_shard, con
                                 float* dH_partial, void* dW_shard, void* workspace,
                                 size_t workspace_bytes, size_t chunk_budget_bytes, void* stream);
 
+/* Host-to-device staging, for callers that feed the entry points from host buffers
+ * (the pages' methods take their inputs already on the device; this is I/O around them).
+ * Copies `bytes` from pinned host memory `src` (page-locked by cudaHostAlloc /
+ * cudaMallocHost or cudaHostRegister, so it has a device mapping) to device memory `dst`,
+ * enqueued on `stream` as one kernel whose threads read the host buffer through that
+ * mapping over the CPU-GPU link and store 16-byte words (the last bytes % 16 one by one).
+ * It is meant to run on a second stream beside the library's kernels, the next step's
+ * inputs arriving while this step computes: it uses no shared memory and few registers,
+ * so its blocks fit beside the tensor-core kernels' one block per SM.  On GB300 a
+ * copy-engine transfer (cudaMemcpyAsync) of the same bytes from host memory slowed those
+ * kernels several times more (a 1 GB copy per 20 ms step: +1.6-2.0 ms against +0.3 ms).
+ * Both pointers 16-byte aligned, else FLCE_ERR_ALIGN.  FLCE_ERR_ARG, nothing enqueued: a
+ * null pointer (with bytes > 0), a src that is not page-locked host memory (pageable
+ * memory is refused even where the GPU could reach it through address translation), or a
+ * dst that is not device memory of the current device.  bytes == 0: FLCE_OK, nothing
+ * enqueued.  The host buffer must stay allocated, and unchanged, until
+ * the copy has run (stream order). */
+FLCE_API flce_status flce_stage_h2d(void* dst, const void* src, size_t bytes, void* stream);
+
 /* Failure-detection self-test.  The pages have no counterpart: it checks the device-side
  * bounded waits that keep a broken pipeline from hanging the GPU.  Launches one kernel
  * whose thread waits, with the same bounded mbarrier wait the tensor-core kernels use
@@ -304,6 +323,7 @@ FLCE_API int flce_last_cuda_error(void);
 #define FLCE_KERNEL_DH_COMBINE 15  /* dH split: fp32 part sums added in part order        */
 #define FLCE_KERNEL_COMPACT 16     /* backward: rows with a gradient gathered to the front  */
 #define FLCE_KERNEL_DH_ZERO 17     /* backward: zero dH rows that carry no gradient         */
+#define FLCE_KERNEL_STAGE 18       /* flce_stage_h2d: pinned host buffer -> device memory   */
 FLCE_API uint64_t flce_launch_count(void);
 FLCE_API int flce_set_event_sink(void* const* start_events, void* const* end_events, int* kernel_ids,
                         int capacity);

@@ -30,14 +30,14 @@ __all__ = [
     "linear_cross_entropy", "FusedLinearCrossEntropyLoss", "flce_forward", "flce_backward", "flce_forward_shard", "flce_merge_shards",
     "flce_backward_shard", "forward_workspace_size",
     "backward_workspace_size", "vocab_order", "FlceError", "check_counts", "check_pending", "library",
-    "launch_count", "EventSink", "KERNEL_NAMES",
+    "launch_count", "EventSink", "KERNEL_NAMES", "stage_h2d",
 ]
 
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 KERNEL_NAMES = {0: "label_dot", 1: "linear_lse", 2: "lse_merge", 3: "reduce", 4: "bwd_prep",
                 5: "dz", 6: "dw", 7: "dh", 8: "zero", 9: "block_mask", 10: "selftest", 11: "shard_merge",
                 12: "vocab_keys", 13: "vocab_sort", 14: "gather", 15: "dh_combine", 16: "compact",
-                17: "dh_zero"}
+                17: "dh_zero", 18: "stage"}
 BWD_SORT_VOCAB = 1
 BWD_COMPENSATED = 2
 
@@ -96,6 +96,8 @@ def library() -> ctypes.CDLL:
             lib.flce_backward_shard.restype = i32
             lib.flce_selftest_wait_timeout.argtypes = [vp, vp]
             lib.flce_selftest_wait_timeout.restype = i32
+            lib.flce_stage_h2d.argtypes = [vp, vp, sz, vp]
+            lib.flce_stage_h2d.restype = i32
             _lib = lib
     return _lib
 
@@ -429,6 +431,26 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
     def extra_repr(self):
         return "ignore_index=%d, softcap=%g, reduction=%s, filter_threshold=%g, sort_vocab=%s, compensated=%s" % (
             self.ignore_index, self.softcap, self.reduction, self.filter_threshold, self.sort_vocab, self.compensated)
+
+
+def stage_h2d(dst, src):
+    """Copy the pinned host tensor `src` into the device tensor `dst` (same byte size,
+    both contiguous) on the current stream of dst's device, by SM loads through the host
+    buffer's device mapping (flce_stage_h2d) rather than the copy engine: meant for a side
+    stream that brings the next step's inputs in while this step's kernels run, which a
+    copy-engine transfer from host memory slows several times more.  Returns dst."""
+    if not dst.is_cuda or src.is_cuda:
+        raise FlceError("stage_h2d copies a host tensor into a CUDA tensor")
+    if not src.is_pinned():
+        raise FlceError("stage_h2d needs a pinned host tensor (pin_memory())")
+    if not (dst.is_contiguous() and src.is_contiguous()):
+        raise FlceError("stage_h2d needs contiguous tensors")
+    nbytes = dst.numel() * dst.element_size()
+    if nbytes != src.numel() * src.element_size():
+        raise FlceError("stage_h2d: %d bytes into %d" % (src.numel() * src.element_size(), nbytes))
+    with torch.cuda.device(dst.device):
+        _check(library().flce_stage_h2d(_p(dst), ctypes.c_void_p(src.data_ptr()), nbytes, _stream(dst.device)))
+    return dst
 
 
 def launch_count() -> int:

@@ -901,6 +901,37 @@ flce_status flce_backward_shard(const void* H, const void* W_shard, const int64_
                        workspace_bytes, chunk_budget_bytes, stream);
 }
 
+flce_status flce_stage_h2d(void* dst, const void* src, size_t bytes, void* stream) {
+  if (bytes == 0) return FLCE_OK;
+  if (!dst || !src) return FLCE_ERR_ARG;
+  if (!aligned(dst, 16) || !aligned(src, 16)) return FLCE_ERR_ALIGN;
+  int sms = 0;
+  flce_status s = device_setup(&sms);
+  if (s != FLCE_OK) return s;
+  // src: page-locked host memory (pageable memory is reachable from the GPU on systems
+  // with address translation services too, but is refused); dst: this device's memory
+  int dev = 0;
+  cudaPointerAttributes as{}, ad{};
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaPointerGetAttributes(&as, src) != cudaSuccess ||
+      cudaPointerGetAttributes(&ad, dst) != cudaSuccess) {
+    (void)cudaGetLastError();  // clear the (non-sticky) lookup error
+    return FLCE_ERR_ARG;
+  }
+  if (as.type != cudaMemoryTypeHost || as.devicePointer == nullptr) return FLCE_ERR_ARG;
+  if ((ad.type != cudaMemoryTypeDevice && ad.type != cudaMemoryTypeManaged) || ad.device != dev) return FLCE_ERR_ARG;
+  const void* dsrc = as.devicePointer;
+  if (!aligned(dsrc, 16)) return FLCE_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t n16 = static_cast<int64_t>(bytes / 16);
+  const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((n16 + kStageThreads - 1) / kStageThreads, sms)));
+  const cudaError_t e = launch(FLCE_KERNEL_STAGE, st, [&] {
+    k_stage_h2d<<<blocks, kStageThreads, 0, st>>>(static_cast<const uint4*>(dsrc), static_cast<uint4*>(dst), n16,
+                                                  static_cast<int>(bytes % 16));
+    return cudaGetLastError();
+  });
+  return e == cudaSuccess ? FLCE_OK : cuda_fail(e);
+}
+
 flce_status flce_selftest_wait_timeout(int64_t* status_word, void* stream) {
   if (!status_word) return FLCE_ERR_ARG;
   if (!aligned(status_word, 8)) return FLCE_ERR_ALIGN;

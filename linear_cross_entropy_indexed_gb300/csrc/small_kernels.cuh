@@ -177,6 +177,30 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ------------------------------------------------------------------ host-to-device staging
+// Grid-stride copy of n16 16-byte words from a pinned host buffer (read through its
+// device mapping) to device memory, four independent loads in flight per thread; block 0
+// copies the last `tail` (< 16) bytes one by one.
+constexpr int kStageThreads = 128;
+__global__ void __launch_bounds__(kStageThreads)
+    k_stage_h2d(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n16, int tail) {
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * step < n16; i += 4 * step) {
+    const uint4 a = src[i];
+    const uint4 b = src[i + step];
+    const uint4 c = src[i + 2 * step];
+    const uint4 d = src[i + 3 * step];
+    dst[i] = a;
+    dst[i + step] = b;
+    dst[i + 2 * step] = c;
+    dst[i + 3 * step] = d;
+  }
+  for (; i < n16; i += step) dst[i] = src[i];
+  if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < tail)
+    reinterpret_cast<uint8_t*>(dst + n16)[threadIdx.x] = reinterpret_cast<const uint8_t*>(src + n16)[threadIdx.x];
+}
+
 // ------------------------------------------------------------------ row compaction
 // The backward runs only on the rows that carry a gradient (scale != 0: a valid label and
 // a non-zero upstream gradient); every other row's dZ row, dH row and share of dW are
