@@ -12,6 +12,7 @@ constexpr int kDotMaxBlocks = 2048; // grid cap (grid-stride beyond)
 constexpr int kMergeThreads = 256;
 constexpr int kMergeRows = 32;     // rows per block of the (m, s) merge: one per lane
 constexpr int kMergeSlices = 8;    // warps per merge block: each merges every 8th partial
+constexpr int kMergeBatch = 16;    // partials a warp loads before merging them
 
 __device__ __forceinline__ float softcap_exact(float x, float c) {
   return c > 0.0f ? c * tanhf(x / c) : x;
@@ -109,9 +110,22 @@ __global__ void __launch_bounds__(kMergeRows * kMergeSlices)
   const int64_t i = static_cast<int64_t>(blockIdx.x) * kMergeRows + lane;
   float m = -INFINITY, s = 0.0f;
   if (i < N) {
-#pragma unroll 4
-    for (int g = slice; g < n_groups; g += kMergeSlices)
-      merge_ms(m, s, part_m[static_cast<int64_t>(g) * N + i], part_s[static_cast<int64_t>(g) * N + i]);
+    // kMergeBatch groups of the slice at a time: all their loads are issued (past the last
+    // group, the batch's first group is read again and dropped) before the merges, which
+    // run in increasing group order as ever
+    for (int g0 = slice; g0 < n_groups; g0 += kMergeBatch * kMergeSlices) {
+      float bm[kMergeBatch], bs[kMergeBatch];
+#pragma unroll
+      for (int b = 0; b < kMergeBatch; ++b) {
+        const int g = g0 + b * kMergeSlices;
+        const int64_t at = static_cast<int64_t>(g < n_groups ? g : g0) * N + i;
+        bm[b] = part_m[at];
+        bs[b] = part_s[at];
+      }
+#pragma unroll
+      for (int b = 0; b < kMergeBatch; ++b)
+        if (g0 + b * kMergeSlices < n_groups) merge_ms(m, s, bm[b], bs[b]);
+    }
   }
   sm[slice][lane] = m;
   ss[slice][lane] = s;
