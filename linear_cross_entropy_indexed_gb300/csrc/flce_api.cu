@@ -497,8 +497,9 @@ flce_status forward_impl(const void* H, const void* W, const int64_t* labels, in
   // (3) fixed-order merge, per-row loss, block sums
   float* loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : nullptr;
   e = launch(FLCE_KERNEL_LSE_MERGE, st, [&] {
-    k_lse_merge<<<pl.merge_blocks, kMergeRows * kMergeSlices, 0, st>>>(part_m, part_s, pl.n_groups * kEpiSplit, N, t_ws, labels,
-                                                           ignore_index, V_total, lse, loss_rows, sums);
+    const auto merge = pl.merge_blocks <= 2 * sms ? k_lse_merge<true> : k_lse_merge<false>;
+    merge<<<pl.merge_blocks, kMergeRows * kMergeSlices, 0, st>>>(part_m, part_s, pl.n_groups * kEpiSplit, N, t_ws,
+                                                                 labels, ignore_index, V_total, lse, loss_rows, sums);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return cuda_fail(e);

@@ -12,7 +12,7 @@ constexpr int kDotMaxBlocks = 2048; // grid cap (grid-stride beyond)
 constexpr int kMergeThreads = 256;
 constexpr int kMergeRows = 32;     // rows per block of the (m, s) merge: one per lane
 constexpr int kMergeSlices = 8;    // warps per merge block: each merges every 8th partial
-constexpr int kMergeBatch = 16;    // partials a warp loads before merging them
+constexpr int kMergeBatch = 16;    // partials a warp loads before merging them (short grids)
 
 __device__ __forceinline__ float softcap_exact(float x, float c) {
   return c > 0.0f ? c * tanhf(x / c) : x;
@@ -99,6 +99,11 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float mg, float sg)
   m = mn;
 }
 
+// BATCH (short grids, at most two blocks per SM): a warp issues the loads of kMergeBatch
+// partials before merging them, since its own loads are all that hides the latency; else
+// it streams them (with enough blocks resident, occupancy hides it and the batch's
+// registers only lower occupancy).  Both merge in the same order: bitwise the same result.
+template <bool BATCH>
 __global__ void __launch_bounds__(kMergeRows * kMergeSlices)
     k_lse_merge(const float* __restrict__ part_m, const float* __restrict__ part_s, int n_groups,
                 int64_t N, const float* __restrict__ t, const int64_t* __restrict__ labels,
@@ -109,7 +114,11 @@ __global__ void __launch_bounds__(kMergeRows * kMergeSlices)
   const int slice = threadIdx.x >> 5;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * kMergeRows + lane;
   float m = -INFINITY, s = 0.0f;
-  if (i < N) {
+  if (i < N && !BATCH) {
+#pragma unroll 4
+    for (int g = slice; g < n_groups; g += kMergeSlices)
+      merge_ms(m, s, part_m[static_cast<int64_t>(g) * N + i], part_s[static_cast<int64_t>(g) * N + i]);
+  } else if (i < N) {
     // kMergeBatch groups of the slice at a time: all their loads are issued (past the last
     // group, the batch's first group is read again and dropped) before the merges, which
     // run in increasing group order as ever
