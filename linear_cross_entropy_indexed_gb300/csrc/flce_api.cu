@@ -44,8 +44,8 @@ constexpr int kPlanPairs = 76;   // SM pairs of a GB300 (152 SMs), for the plann
 constexpr int kBandM = 16;
 // bf16 dZ chunk bytes.  Measured sustained on one GB300 (forward + backward per step,
 // 100-step runs at the power cap): 512 MiB runs the Llama-3-, Gemma-2- and packed-shaped
-// heads within 0.5% of 1 GiB for 44-47% less peak extra memory; 384 and 256 MiB cost
-// 0.6-1.7% and 1.1-2.7% (more launches, each with its own ramp and tail).
+// heads within 0.7-1.0% of 1 GiB for 27-45% less peak extra memory; 384 and 256 MiB cost
+// 0.5-1.7% and 1.1-2.1% more (more launches, and a dH read-modify-write per chunk).
 constexpr size_t kDefaultChunkBudget = size_t(512) << 20;
 constexpr int kMaxDevices = 64;
 
