@@ -19,7 +19,6 @@ from __future__ import annotations
 
 import argparse
 import datetime
-import glob
 import hashlib
 import json
 import os

@@ -9,7 +9,6 @@ backward.  Vocab-parallel: each rank holds a vocabulary shard, computes
 per-row (max, sum, target) over it, and the ranks merge them in rank order with the
 running (m, s) rule (ai-infra-kb M011 §05 and §07); the merged LSE and loss must equal
 the unsharded oracle."""
-import os
 import socket
 
 import numpy as np

@@ -10,7 +10,6 @@ import numpy as np
 import pytest
 import torch
 
-import oracle as O
 import synthetic as S
 from tests import parity as P
 

@@ -3,7 +3,6 @@ out (an mbarrier that nothing arrives on) and must return with the error bit set
 after which the context still runs the fused loss correctly."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 

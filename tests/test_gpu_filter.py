@@ -9,7 +9,6 @@ property of the method, not of the kernels)."""
 import numpy as np
 import pytest
 
-import oracle as O
 import synthetic as S
 from tests import parity as P
 

@@ -10,7 +10,6 @@ before anything runs.  It lives in a file of its own that pytest collects last a
 self-contained, so it passes alone in a fresh process and after the other tests."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
