@@ -374,8 +374,10 @@ def test_widen_bf16():
 # ------------------------------------------------------------------ planted mistakes
 ALL_PINS = [pin_worked_example, pin_two_tile_split, pin_torch_library,
             lambda: pin_torch_library(softcap=2.0), lambda: pin_torch_library(red="none"),
+            lambda: pin_torch_library(red="sum"),
             pin_finite_differences, lambda: pin_finite_differences(softcap=1.5),
-            pin_closed_forms, pin_split_invariance, pin_label_conventions, pin_widen_bf16]
+            pin_closed_forms, pin_split_invariance, pin_label_conventions, pin_widen_bf16,
+            lambda: pin_filtered_backward()]
 
 
 def _caught():
@@ -392,6 +394,7 @@ def _caught():
 def _mutants():
     orig_lse, orig_cap_grad, orig_dl, orig_raw = O._lse, O._cap_grad, O._dlogits, O._raw_logits
     orig_scale, orig_merge, orig_status = O.row_scale, O.merge, O.label_status
+    orig_dh_rows, orig_target_rows = O.dH_rows, O.target_rows
 
     def lse_no_shift(Z):                       # dropped max subtraction
         return np.log(np.exp(Z).sum(axis=1))
@@ -432,17 +435,39 @@ def _mutants():
     def widen_as_fp16(bits):                   # read as IEEE half precision instead of bf16
         return np.asarray(bits).astype(np.uint16).view(np.float16).astype(np.float64)
 
+    def scale_sum_as_mean(valid, n_valid, red, g):  # the sum reduction divided by the valid count
+        return orig_scale(valid, n_valid, "mean" if red == "sum" else red, g)
+
+    def cap_inner_unscaled(X, c):              # c tanh(x) instead of c tanh(x / c)
+        return c * np.tanh(X) if c > 0 else X
+
+    def filter_drops_target(P, labels, valid, thr):  # the target entry filtered like the rest
+        return np.where(P >= thr, P, 0.0) if thr > 0 else P
+
+    def dh_rows_local_count(Hf, Wf, labels, lse, rows, *a, n_valid=None, **k):  # count of the sample only
+        lab = np.asarray(labels)
+        return orig_dh_rows(Hf, Wf, labels, lse, rows, *a, n_valid=int((lab[np.asarray(rows)] != -100).sum()), **k)
+
+    def tile_sum_unshifted(Z):                 # sum of exp(z), not of exp(z - m)
+        return Z.max(axis=1), np.exp(Z).sum(axis=1)
+
+    def target_uncapped(Hf, Wf, labels, rows, ignore_index=-100, softcap=0.0):  # target before the cap
+        return orig_target_rows(Hf, Wf, labels, rows, ignore_index, 0.0)
+
     return [("_lse", lse_no_shift), ("_lse", lse_max_only), ("_cap_grad", cap_grad_one),
             ("_dlogits", dl_wrong_sign), ("_raw_logits", raw_reversed), ("row_scale", scale_by_rows),
             ("merge", merge_no_rescale), ("label_status", status_no_range),
-            ("widen_bf16", widen_shift8), ("widen_bf16", widen_byteswap), ("widen_bf16", widen_as_fp16)]
+            ("widen_bf16", widen_shift8), ("widen_bf16", widen_byteswap), ("widen_bf16", widen_as_fp16),
+            ("row_scale", scale_sum_as_mean), ("_cap", cap_inner_unscaled), ("_filter", filter_drops_target),
+            ("dH_rows", dh_rows_local_count), ("tile_stats", tile_sum_unshifted),
+            ("target_rows", target_uncapped)]
 
 
 def test_pins_pass_on_the_oracle():
     assert _caught() == 0
 
 
-@pytest.mark.parametrize("mutant", range(11))
+@pytest.mark.parametrize("mutant", range(17))
 def test_planted_mistake_is_caught(mutant, monkeypatch):
     name, fn = _mutants()[mutant]
     monkeypatch.setattr(O, name, fn)
@@ -450,7 +475,7 @@ def test_planted_mistake_is_caught(mutant, monkeypatch):
 
 
 # ------------------------------------------------------------------ gradient filtering
-def test_filtered_backward_pins():
+def pin_filtered_backward():
     """threshold 0 is the exact gradient; a threshold above every probability keeps only
     the target entries, whose closed form is dH_i = (p_iy - 1) s_i w_y and
     dW_v = sum over rows with y_i = v of (p_iy - 1) s_i h_i; an intermediate threshold
@@ -489,6 +514,10 @@ def test_filtered_backward_pins():
                                atol=1e-15)
     vs = np.array([0, 4, 22])
     np.testing.assert_allclose(O.dW_rows(H, W, y, f.lse, vs, filter_threshold=thr), dW2[vs], rtol=1e-12, atol=1e-15)
+
+
+def test_filtered_backward_pins():
+    pin_filtered_backward()
 
 
 # ------------------------------------------------------------------ vocabulary order
